@@ -1,0 +1,361 @@
+"""Benchmark of one step of the paged-KV-cache hot path on GB300.
+
+A step = pkv_write (this step's new K/V rows into the pool) + pkv_attend
+(paged GQA attention of every query row) over one batch of the
+Llama-3-8B-shaped decode workload: 64 sequences, context lengths uniform in
+[512, 4096], 32 query / 8 KV heads, head_dim 128, 16-token pages shuffled in a
+pool 1.25x the need, bf16 N(0,1) values from a fixed seed.
+
+Prints ONE JSON line (rank 0).  value = decode tokens/s of the whole job
+(query rows per step x steps / time, max over ranks).  The pool (~0.75 GB) is
+larger than L2 and L2 is also flushed (256 MiB write) before every timed step,
+outside the step's CUDA-event pair.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload IDX]
+        python bench.py --impl reference ...   (float64 CPU oracle, same metric)
+Multi-GPU: launched under torchrun, every rank runs an independent replica
+(sequences are independent; there is no exchange step).
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "decode tokens/s and achieved HBM GB/s (fraction of 8 TB/s) per attend step, 1×GB300"
+NOMINAL_HBM_GBS = 8000.0
+KERNEL_SOURCES = ["paged_kv_cache_pkv_gb300/csrc/pkv_decode.cu",
+                  "paged_kv_cache_pkv_gb300/csrc/pkv_common.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    return ap.parse_args()
+
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend)
+    return rank, world, local
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled while the timed loop runs."""
+
+    Q = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+         "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.lines, self.proc, self.bus = [], None, None
+        try:
+            self.bus = torch.cuda.get_device_properties(device).pci_bus_id
+        except Exception:
+            self.bus = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader",
+                                          "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.7)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [[c.strip() for c in l.split(",")] for l in self.lines if l.count(",") >= 10]
+        if self.bus:
+            mine = [r for r in rows if self.bus.lower()[-12:] in r[1].lower()]
+            rows = mine or rows
+        if not rows:
+            return None
+        num = lambda s: float(s.split()[0]) if s and s.split()[0].replace(".", "").isdigit() else None
+        loaded = [r for r in rows if (num(r[5]) or 0) > 0] or rows
+        sm = [num(r[2]) for r in loaded if num(r[2]) is not None]
+        reasons = set()
+        for r in loaded:
+            for name, col in (("hw_slowdown", 7), ("hw_thermal_slowdown", 8),
+                              ("sw_thermal_slowdown", 9), ("sw_power_cap", 10)):
+                if r[col].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][3]), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max((num(r[4]) or 0) for r in rows)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle as CPU baseline / reference arm
+# ---------------------------------------------------------------------------
+def oracle_sample(batch, max_rows, min_seconds=0.0, max_reps=50):
+    """Time the float64 oracle (write + attend) on the first ``max_rows`` query
+    rows of the batch, single-threaded; returns (tokens/s, rows, seconds)."""
+    import oracle.pkv_oracle as O
+    b16 = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    q, kn, vn = b16(batch.q), b16(batch.k_new), b16(batch.v_new)
+    kc, vc = b16(batch.k_cache), b16(batch.v_cache)
+    rows = list(range(min(max_rows, batch.T)))
+    total, reps, t0 = 0.0, 0, time.perf_counter()
+    while True:
+        s = time.perf_counter()
+        k2, v2 = O.write(kn, vn, batch.slot_mapping, kc, vc, batch.page_size)
+        O.attend(q, k2, v2, batch.block_tables, batch.seq_lens, batch.query_start_loc, batch.scale,
+                 batch.num_q_heads, batch.num_kv_heads, batch.page_size, rows=rows)
+        total += time.perf_counter() - s
+        reps += 1
+        if time.perf_counter() - t0 >= min_seconds or reps >= max_reps:
+            break
+    return len(rows) * reps / total, len(rows), total
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from workloads import workload
+    b = workload(args.workload, device="cpu")
+    steps, warm = args.steps, args.warmup
+    # each step: the oracle over a bounded sample (4 rows) of the workload
+    rows = 4
+    times = []
+    for i in range(warm + steps):
+        s = time.perf_counter()
+        rate, n, _ = oracle_sample(b, rows, max_reps=1)
+        if i >= warm:
+            times.append(time.perf_counter() - s)
+        if i >= warm and sum(times) > 120:
+            break
+    done = len(times)
+    value = rows * done / sum(times)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": done, "warmup": warm, "ms_per_step": 1e3 * sum(times) / done,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(b, args.workload),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{rows} query rows (with the full write) of the workload per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(b, idx):
+    from workloads import WORKLOADS
+    return {"workload": f"cfg{idx}: {WORKLOADS[idx]}", "num_seqs": b.B, "query_rows": b.T,
+            "num_q_heads": b.num_q_heads, "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim,
+            "page_size": b.page_size, "pool_pages": b.num_blocks,
+            "context_tokens": int(b.seq_lens.astype(np.int64).sum()),
+            "l2": "pool larger than L2; 256 MiB L2 flush before every timed step (outside its events)"}
+
+
+# ---------------------------------------------------------------------------
+# the library
+# ---------------------------------------------------------------------------
+def main():
+    args = parse()
+    rank, world, local = dist_init(args)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import paged_kv_cache_pkv_gb300 as pkv
+    from workloads import kv_bytes, workload
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    b = workload(args.workload, device=dev)
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).to(dev)
+    slots, bt, lens, qsl = (t(b.slot_mapping, np.int64), t(b.block_tables, np.int32),
+                            t(b.seq_lens, np.int32), t(b.query_start_loc, np.int32))
+    kc, vc = b.k_cache, b.v_cache
+    out = torch.empty_like(b.q)
+    desc = pkv.make_desc(kc, b.num_q_heads, bt.shape[1])
+    ws = torch.empty(pkv.workspace_size(desc, b.B, b.T, dev), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pkv.write(b.k_new, b.v_new, slots, kc, vc)
+        pkv.attend(b.q, kc, vc, bt, lens, qsl, b.scale, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if pkv.get_last_error():
+        raise RuntimeError("device status flags set during warm-up")
+
+    clocks = ClockSampler(dev)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    trace = pkv.Trace(capacity=args.steps * 8 + 16)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = pkv.launch_count()
+    with trace:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    launches = pkv.launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(c) for a, c in ev]
+    total_s = sum(step_ms) / 1e3
+    if world > 1:
+        x = torch.tensor([total_s], device=dev)
+        torch.distributed.all_reduce(x, op=torch.distributed.ReduceOp.MAX)
+        total_s = float(x.item())
+    if pkv.get_last_error():
+        raise RuntimeError("device status flags set during the timed region")
+
+    tokens = b.T * args.steps * world
+    value = tokens / total_s
+    uniq = kv_bytes(b, unique=True)
+    qo_bytes = 2 * b.q.numel() * 2
+    meta_bytes = 4 * (b.block_tables.size + 2 * b.B + 1)
+    alg_bytes = uniq + qo_bytes + meta_bytes
+    dec_ms, dec_n = trace.read("decode")
+    dec_avg_s = dec_ms / max(dec_n, 1) / 1e3
+    peaks, peak_kind = measured_peaks()
+    achieved = alg_bytes / dec_avg_s / 1e9
+    traffic = None
+    try:
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        if tr.get("kernel_hash") == kernel_hash() and tr.get("workload") == args.workload:
+            traffic = tr.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    per_kernel = {}
+    for k in ("write", "plan", "decode", "merge", "prefill"):
+        ms, n = trace.read(k)
+        if n:
+            per_kernel[k] = {"launches": n, "avg_us": 1e3 * ms / n}
+
+    # ---- end to end through the public API with host buffers ----
+    e2e_steps = min(args.e2e_steps, max(args.steps, 1))
+    host = {name: x.cpu().pin_memory() for name, x in
+            (("q", b.q), ("k_new", b.k_new), ("v_new", b.v_new), ("slots", slots), ("bt", bt),
+             ("lens", lens), ("qsl", qsl))}
+    dev_in = {name: torch.empty_like(x, device=dev) for name, x in host.items()}
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(x.numel() * x.element_size() for x in host.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for name, x in host.items():
+            dev_in[name].copy_(x, non_blocking=True)
+        pkv.write(dev_in["k_new"], dev_in["v_new"], dev_in["slots"], kc, vc)
+        pkv.attend(dev_in["q"], kc, vc, dev_in["bt"], dev_in["lens"], dev_in["qsl"], b.scale, out=out,
+                   workspace=ws)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        flush.zero_()
+        e_ev[i][0].record(stream)
+        e2e_step()
+        e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_s = sum(a.elapsed_time(c) for a, c in e_ev) / 1e3
+    if world > 1:
+        x = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(x, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(x.item())
+    e2e_value = b.T * e2e_steps * world / e2e_s
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, rows, secs = oracle_sample(b, b.T, min_seconds=10.0)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"all {rows} query rows of one step (write + attend), repeated for {secs:.1f} s, "
+                         "single-threaded NumPy float64"}
+
+    if rank == 0:
+        ms_per_step = 1e3 * total_s / args.steps
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(b, args.workload),
+            "hbm": {"unique_kv_bytes": uniq, "logical_kv_bytes": kv_bytes(b, unique=False),
+                    "step_gbs": alg_bytes / (total_s / args.steps / world) / 1e9,
+                    "step_frac_of_8tbs": alg_bytes / (total_s / args.steps / world) / 1e9 / NOMINAL_HBM_GBS,
+                    "decode_kernel_frac_of_8tbs": achieved / NOMINAL_HBM_GBS},
+            "roofline": {"bound": "hbm", "kernel": "pkv_decode_kernel", "achieved": achieved,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "peak_kind": peak_kind, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": alg_bytes,
+                         "avg_launch_us": dec_avg_s * 1e6},
+            "kernels": per_kernel,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    trace.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

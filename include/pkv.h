@@ -1,0 +1,183 @@
+/*
+ * pkv.h -- C ABI of the paged-KV-cache hot path for one GB300 (sm_103a).
+ *
+ * Two calls do the per-step work of a continuous batch:
+ *   pkv_write   scatters this step's new K/V rows into fixed-size pages of a
+ *               pool through a slot mapping;
+ *   pkv_attend  runs grouped-query attention for every query row of the
+ *               batch (decode rows and chunked-prefill rows alike), reading
+ *               K/V through each sequence's block table.
+ *
+ * What the method is (sources: the pages this library is built from):
+ *   - llm-d blog post "What does production-grade LLM inference look like?",
+ *     introduction: serving engines keep a KV cache and raise throughput with
+ *     paged attention and continuous batching; decode is memory-bandwidth
+ *     bound, prefill compute bound.  Its routing-factor and prefix-producer
+ *     paragraphs: a prompt whose prefix KV is already cached skips that
+ *     prefill, i.e. cached pages are reused by later requests.
+ *   - vLLM notes "EngineCoreClient: dos caminos de cliente, en proceso y
+ *     multiproceso", "Flujo de datos": the engine reports num_gpu_blocks and
+ *     the aligned block_size it reserved -> a pool of fixed-size pages.
+ *   - TensorRT Edge-LLM "HTTP Inference Server Architecture", "Request
+ *     Lifecycle" and "Extension Rules": the native runtime owns retained
+ *     pages under a single-writer contract.
+ * The pages give no layout, formula or kernel; the readings below are this
+ * library's (pool layout, bottom-right causal alignment, kv head h/(Hq/Hkv)).
+ *
+ * Conventions for every call
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *     contiguous, row-major, 16-byte aligned; the caller owns them and keeps
+ *     them alive until the stream has passed the call (the calls are
+ *     stream-ordered and never synchronise or copy device->host).
+ *   - The library allocates no device memory.  pkv_attend takes a
+ *     caller-provided workspace sized by pkv_attend_workspace_size.
+ *   - bf16 data are passed as raw 16-bit patterns (pkv_bf16).
+ *   - Return value: PKV_OK (0) or a negative PKV_ERR_* code.  On an argument
+ *     error nothing is launched.  Problems only the device can see (a page id
+ *     outside the pool, a query count above its sequence length, a bounded
+ *     wait that ran out) set bits of a per-device status word that
+ *     pkv_get_last_error reads; results of such a call are undefined, but
+ *     no out-of-bounds access is made and no kernel hangs.
+ *   - The caller is the single writer of the pool: a slot written by
+ *     pkv_write must lie in a page that belongs to one sequence only (pages
+ *     shared through a common prefix are read-only), and no two tokens of
+ *     one call may name the same slot.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t pkv_bf16;                 /* raw bfloat16 bits             */
+typedef struct CUstream_st* pkv_stream_t;  /* same handle as cudaStream_t   */
+typedef struct CUevent_st* pkv_event_t;    /* same handle as cudaEvent_t    */
+
+/* ---- return codes --------------------------------------------------------- */
+#define PKV_OK              0
+#define PKV_ERR_NULL       (-1)  /* a required pointer is NULL                   */
+#define PKV_ERR_ALIGN      (-2)  /* a pointer is not aligned as required         */
+#define PKV_ERR_SHAPE      (-3)  /* unsupported head_dim / page_size / heads     */
+#define PKV_ERR_RANGE      (-4)  /* a count or size is out of range              */
+#define PKV_ERR_WORKSPACE  (-5)  /* workspace smaller than required              */
+#define PKV_ERR_LAUNCH     (-6)  /* a CUDA launch or runtime call failed         */
+#define PKV_ERR_DEVICE     (-7)  /* current device is not an sm_103 GPU          */
+#define PKV_ERR_STATE      (-8)  /* misuse of the trace API                      */
+
+/* ---- device status bits (pkv_get_last_error) ------------------------------- */
+#define PKV_STATUS_BAD_SLOT   0x1u  /* slot_mapping entry beyond the pool: skipped */
+#define PKV_STATUS_BAD_BLOCK  0x2u  /* block_tables entry outside [0,num_blocks)  */
+#define PKV_STATUS_BAD_QUERY  0x4u  /* query_start_loc/seq_lens inconsistent      */
+#define PKV_STATUS_TIMEOUT    0x8u  /* a bounded wait in a kernel ran out         */
+
+/* Page-pool and head geometry, checked on every call.
+ *   k_cache and v_cache are each [num_blocks, num_kv_heads, page_size, head_dim]
+ *   bf16: one (page, kv head) is page_size*head_dim contiguous values (4 KiB
+ *   for 16 x 128), so a page of one head is a single contiguous copy.
+ *   block_tables is [num_seqs, max_blocks_per_seq] int32.
+ * Supported: head_dim == 128, page_size == 16, num_q_heads a multiple of
+ * num_kv_heads with num_q_heads/num_kv_heads in {1, 2, 4, 8, 16}. */
+typedef struct {
+  int32_t num_blocks;          /* pages in the pool (vLLM's num_gpu_blocks)   */
+  int32_t page_size;           /* tokens per page (vLLM's block_size)         */
+  int32_t num_kv_heads;        /* Hkv                                         */
+  int32_t num_q_heads;         /* Hq                                          */
+  int32_t head_dim;            /* D                                           */
+  int32_t max_blocks_per_seq;  /* row stride of block_tables                  */
+} pkv_desc;
+
+/* pkv_write -- scatter new K/V rows into the pool (KV write step).
+ *   k_new, v_new   [num_tokens, num_kv_heads, head_dim] bf16, device.
+ *   slot_mapping   [num_tokens] int64, device.  Token t goes to page
+ *                  slot/page_size, row slot%page_size, for every kv head.
+ *                  slot < 0: token skipped (padding).  A slot at or beyond
+ *                  num_blocks*page_size is skipped and flags
+ *                  PKV_STATUS_BAD_SLOT.
+ *   k_cache, v_cache  pools, device, updated in place.
+ *   num_tokens     >= 0; 0 launches nothing.
+ * The copy is bit-exact. */
+PKV_API int pkv_write(const pkv_bf16* k_new, const pkv_bf16* v_new,
+              const int64_t* slot_mapping, int64_t num_tokens,
+              pkv_bf16* k_cache, pkv_bf16* v_cache,
+              const pkv_desc* desc, pkv_stream_t stream);
+
+/* Workspace bytes pkv_attend needs on the CURRENT device for a batch of up
+ * to num_seqs sequences and num_tokens query rows.  Writes *bytes. */
+PKV_API int pkv_attend_workspace_size(const pkv_desc* desc, int32_t num_seqs,
+                              int32_t num_tokens, size_t* bytes);
+
+/* pkv_attend -- paged grouped-query attention of one continuous batch.
+ *   q             [num_tokens, num_q_heads, head_dim] bf16, device.
+ *   k_cache, v_cache  pools as in pkv_desc (already holding this step's rows).
+ *   block_tables  [num_seqs, max_blocks_per_seq] int32: logical token j of
+ *                 sequence b is in page block_tables[b][j/page_size], row
+ *                 j%page_size.  Entries past a sequence's last page are never
+ *                 read.  Several rows may name the same page (shared prefix).
+ *   seq_lens      [num_seqs] int32: L_b, cached tokens including this step's.
+ *   query_start_loc [num_seqs+1] int32, non-decreasing, [0] == 0,
+ *                 [num_seqs] <= num_tokens: sequence b owns query rows
+ *                 query_start_loc[b] .. query_start_loc[b+1]-1 (n_b rows,
+ *                 n_b <= L_b).  Row j of b is at position L_b-n_b+j and sees
+ *                 keys 0..L_b-n_b+j (bottom-right causal; n_b == 1 is
+ *                 decode over all L_b keys).
+ *   scale         softmax scale applied to q.k (e.g. 1/sqrt(head_dim)).
+ *   out           [num_tokens, num_q_heads, head_dim] bf16, device; rows at
+ *                 or beyond query_start_loc[num_seqs] are not written.
+ *   workspace     device scratch of >= pkv_attend_workspace_size bytes,
+ *                 256-byte aligned; contents need no initialisation.
+ * Query head h reads kv head h / (num_q_heads/num_kv_heads). */
+PKV_API int pkv_attend(const pkv_bf16* q, const pkv_bf16* k_cache,
+               const pkv_bf16* v_cache, const int32_t* block_tables,
+               const int32_t* seq_lens, const int32_t* query_start_loc,
+               int32_t num_seqs, int32_t num_tokens, float scale,
+               pkv_bf16* out, void* workspace, size_t workspace_bytes,
+               const pkv_desc* desc, pkv_stream_t stream);
+
+/* Wait for `stream`, then read and clear the current device's status word
+ * (PKV_STATUS_* bits) into *flags. */
+PKV_API int pkv_get_last_error(pkv_stream_t stream, uint32_t* flags);
+
+/* Human-readable text for a PKV_ERR_* code. */
+PKV_API const char* pkv_strerror(int code);
+
+/* Total kernel launches this process has made through the library. */
+PKV_API uint64_t pkv_launch_count(void);
+
+/* ---- tracing: per-kernel device time, recorded with CUDA events ----------- */
+/* Kernel ids used by the trace. */
+#define PKV_K_WRITE    0
+#define PKV_K_PLAN     1
+#define PKV_K_DECODE   2
+#define PKV_K_MERGE    3
+#define PKV_K_PREFILL  4
+#define PKV_K_COUNT    5
+
+typedef struct pkv_trace pkv_trace;
+/* Create a trace with room for `capacity` launches (creates 2*capacity CUDA
+ * events on the current device; not meant for the hot path). */
+PKV_API int pkv_trace_create(int32_t capacity, pkv_trace** out);
+/* While a trace is attached to the calling thread, every launch the library
+ * makes on that thread records an event before and after it. */
+PKV_API int pkv_trace_attach(pkv_trace* tr);
+PKV_API int pkv_trace_detach(void);
+/* Wait for the recorded events and sum per kernel id: total milliseconds and
+ * number of launches.  Launches beyond the capacity are counted, not timed. */
+PKV_API int pkv_trace_read(pkv_trace* tr, int32_t kernel_id, double* total_ms,
+                   int64_t* launches);
+PKV_API int pkv_trace_reset(pkv_trace* tr);
+PKV_API int pkv_trace_destroy(pkv_trace* tr);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

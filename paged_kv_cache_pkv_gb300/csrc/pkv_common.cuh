@@ -1,0 +1,152 @@
+// pkv_common.cuh -- constants, workspace layout and PTX helpers shared by the
+// paged-KV-cache kernels (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+// Geometry this library is specialised for (checked on every call).
+constexpr int kHeadDim = 128;   // D
+constexpr int kPage = 16;       // tokens per page
+constexpr int kPageBytes = kPage * kHeadDim * 2;  // one (page, kv head): 4 KiB
+
+// Split-KV decode kernel shape.
+constexpr int kDecWarps = 4;     // independent worker warps per CTA
+constexpr int kDecStages = 3;    // pages (K+V) in flight per warp
+constexpr int kMaxGroupPerItem = 4;  // query heads handled per decode item
+
+// A decode partial state: m[4], l[4], then o[GH][128] (fp32).
+constexpr int kPartialHeader = 8;
+__host__ __device__ constexpr int partial_floats(int gh) { return kPartialHeader + gh * kHeadDim; }
+
+// Bounded waits: after this many failed mbarrier polls a kernel gives up,
+// flags PKV_STATUS_TIMEOUT and returns.
+constexpr uint32_t kWaitLimit = 1u << 24;
+
+// Work plan written by the plan kernel into the caller's workspace.
+struct PlanHeader {
+  int32_t units;   // total (row, kv head group, page) units of the split-KV path
+  int32_t chunk;   // units per decode warp
+  int32_t nwarps;  // decode warps the plan was made for
+  int32_t prefill_tiles;  // tensor-core prefill tiles in the tile list
+};
+
+// Workspace carve-up; every piece starts 256-byte aligned.
+struct WorkspaceLayout {
+  size_t header, row_unit_start, row_seq, row_nvis, warp_first_row, tiles, partials, total;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WorkspaceLayout workspace_layout(int num_seqs, int num_tokens, int nwarps, int gh,
+                                        int max_tiles) {
+  WorkspaceLayout w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t at = off; off = align_up(off + bytes, 256); return at; };
+  w.header = take(sizeof(PlanHeader));
+  w.row_unit_start = take(sizeof(int32_t) * (size_t(num_tokens) + 1));
+  w.row_seq = take(sizeof(int32_t) * size_t(num_tokens));
+  w.row_nvis = take(sizeof(int32_t) * size_t(num_tokens));
+  w.warp_first_row = take(sizeof(int32_t) * size_t(nwarps));
+  w.tiles = take(sizeof(int32_t) * 2 * size_t(max_tiles));
+  w.partials = take(sizeof(float) * size_t(partial_floats(gh)) * 2 * size_t(nwarps));
+  w.total = off;
+  (void)num_seqs;
+  return w;
+}
+
+// ---------------------------------------------------------------------------
+// PTX helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for the phase with the given parity; false if the bound ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint32_t limit = kWaitLimit) {
+  for (uint32_t i = 0; i < limit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// L2 policy for data read exactly once (KV pages of a decode step).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Bulk (non-tensor) async copy global -> shared, completing on an mbarrier.
+// dst/src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// bf16x2 (packed in a 32-bit word, element 0 in the low half) -> two floats.
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);  // .x = a (low half), .y = b
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void flag_status(unsigned* status, unsigned bits) {
+  if (status) atomicOr(status, bits);
+}
+
+}  // namespace pkv

@@ -1,0 +1,77 @@
+// pkv_internal.h -- host-side plumbing shared by the translation units of the
+// library: per-device facts, the launch context, launch tracing.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  int dec_ctas_per_sm = 0;   // resident split-KV decode CTAs per SM
+  int dec_warps_total = 0;   // decode warps of one persistent launch
+  size_t smem_optin = 0;
+};
+
+// Facts about the current device (cached; filled on first use per device).
+// Returns nullptr and sets *err when the device is unusable.
+const DeviceInfo* current_device(int* err);
+
+struct LaunchCtx {
+  cudaStream_t stream;
+  const DeviceInfo* dev;
+  unsigned* status;  // device address of this device's status word
+};
+
+// Records a trace event pair around one launch when a trace is attached to
+// the calling thread, and counts the launch.
+class TraceScope {
+ public:
+  TraceScope(cudaStream_t s, int kernel_id);
+  // Call right after the launch: returns PKV_OK or PKV_ERR_LAUNCH.
+  int done();
+
+ private:
+  cudaStream_t stream_;
+  int kernel_;
+  int slot_;
+};
+
+int launch_write(const LaunchCtx& ctx, const uint16_t* k_new, const uint16_t* v_new,
+                 const int64_t* slot_mapping, int64_t num_tokens, uint16_t* k_cache,
+                 uint16_t* v_cache, int32_t num_blocks, int32_t num_kv_heads);
+
+struct AttendArgs {
+  const uint16_t* q;
+  const uint16_t* k_cache;
+  const uint16_t* v_cache;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  int32_t num_seqs, num_tokens;
+  float scale;
+  uint16_t* out;
+  void* workspace;
+  size_t workspace_bytes;
+  pkv_desc desc;
+};
+
+// Workspace bytes for a batch on the current device.
+size_t attend_workspace_bytes(const DeviceInfo& dev, const pkv_desc& d, int32_t num_seqs,
+                              int32_t num_tokens);
+int launch_attend(const LaunchCtx& ctx, const AttendArgs& a);
+
+// Resident CTAs per SM of the decode kernel (occupancy query).
+int decode_ctas_per_sm(int group_per_item);
+
+// Tensor-core chunked-prefill path (pkv_prefill.cu).
+int prefill_max_tiles(const pkv_desc& d, int32_t num_seqs, int32_t num_tokens);
+int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, const void* tiles,
+                   const void* header, int max_tiles);
+
+}  // namespace pkv

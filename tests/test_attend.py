@@ -1,0 +1,178 @@
+"""pkv_attend parity against the float64 oracle (max |err| <= 1e-2, mean <= 1e-3).
+
+Small batches are compared on every output; the full-size named workloads on
+all rows where the oracle is quick and on a sample of rows (shortest, longest,
+first/last prefill rows, random) where it is not.
+"""
+
+import base64
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.pkv_oracle as O
+import paged_kv_cache_pkv_gb300 as pkv
+from helpers import bits, compare, oracle_attend, oracle_write, to_device
+from workloads import make_batch, workload
+
+pytestmark = pytest.mark.gpu
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def run_step(batch, meta=None, out=None):
+    """pkv_write then pkv_attend on a fresh copy of the batch's pools."""
+    meta = meta or to_device(batch)
+    kc, vc = batch.k_cache.clone(), batch.v_cache.clone()
+    pkv.write(batch.k_new, batch.v_new, meta["slot_mapping"], kc, vc)
+    out = pkv.attend(batch.q, kc, vc, meta["block_tables"], meta["seq_lens"],
+                     meta["query_start_loc"], batch.scale, out=out)
+    torch.cuda.synchronize()
+    return out, kc, vc
+
+
+def check_batch(batch, rows=None, what=""):
+    out, kc, vc = run_step(batch)
+    assert pkv.get_last_error() == 0
+    k_ref, v_ref = oracle_write(batch)
+    expected = oracle_attend(batch, k_ref, v_ref, rows=rows)
+    return compare(out, expected, rows=rows, what=what or batch.name)
+
+
+def test_golden_tiny_mixed(pkvlib):
+    g = json.load(open(os.path.join(HERE, "golden", "tiny_mixed.json")))
+    dec = lambda k, dt: np.frombuffer(base64.b64decode(g[k]), dtype=dt)
+    Hq, Hkv, D, P, NB, T = g["num_q_heads"], g["num_kv_heads"], 128, 16, g["num_blocks"], g["T"]
+    t16 = lambda k, shape: torch.from_numpy(dec(k, np.int16).reshape(shape).copy()).view(torch.bfloat16).cuda()
+    q = t16("q", (T, Hq, D))[: g["num_query_rows"]].contiguous()
+    kc, vc = t16("k_cache", (NB, Hkv, P, D)), t16("v_cache", (NB, Hkv, P, D))
+    pkv.write(t16("k_new", (T, Hkv, D)), t16("v_new", (T, Hkv, D)),
+              torch.tensor(g["slot_mapping"], dtype=torch.int64).cuda(), kc, vc)
+    out = pkv.attend(q, kc, vc, torch.tensor(g["block_tables"], dtype=torch.int32).cuda(),
+                     torch.tensor(g["seq_lens"], dtype=torch.int32).cuda(),
+                     torch.tensor(g["query_start_loc"], dtype=torch.int32).cuda(), g["scale"])
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(kc).ravel(), dec("k_cache_after", np.uint16))
+    assert np.array_equal(bits(vc).ravel(), dec("v_cache_after", np.uint16))
+    expected = dec("out_f64", np.float64).reshape(T, Hq, D)[: g["num_query_rows"]]
+    compare(out, expected, what="golden")
+
+
+@pytest.mark.parametrize("idx", [1, 2, 4])
+def test_named_workload_all_rows(pkvlib, idx):
+    check_batch(workload(idx, device="cuda"))
+
+
+def test_long_tail_sampled_rows(pkvlib):
+    b = workload(3, device="cuda")
+    lens = b.seq_lens
+    rng = np.random.default_rng(0)
+    rows = sorted(set([int(np.argmin(lens)), int(np.argmax(lens))] + rng.choice(b.B, 14, replace=False).tolist()))
+    check_batch(b, rows=rows, what="cfg3 sampled")
+
+
+def test_mixed_step_sampled_rows(pkvlib):
+    b = workload(5, device="cuda")
+    qsl = b.query_start_loc
+    pre = [96, 97, 100, 127, 128, 300, 511 + 96, 96 + 512, 96 + 513, 96 + 700, 96 + 1023]
+    rng = np.random.default_rng(1)
+    rows = sorted(set(pre + rng.choice(96, 8, replace=False).tolist()))
+    assert qsl[-1] == 1120
+    check_batch(b, rows=rows, what="cfg5 sampled")
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_small_batches(pkvlib, seed):
+    rng = np.random.default_rng(100 + seed)
+    B = int(rng.integers(1, 9))
+    lens = rng.integers(1, 301, size=B)
+    qlens = np.array([int(rng.integers(1, min(40, L) + 1)) if rng.random() < 0.4 else 1 for L in lens])
+    hq, hkv = [(8, 2), (32, 8), (4, 4), (16, 2), (8, 4)][seed % 5]
+    check_batch(make_batch(lens, qlens, hq, hkv, seed=seed, device="cuda"))
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+def test_group_sizes(pkvlib, G):
+    hkv = 2
+    check_batch(make_batch([33, 250, 16, 1], [1, 1, 16, 1], G * hkv, hkv, seed=40 + G, device="cuda"))
+
+
+def test_zero_length_queries_and_idle_rows(pkvlib):
+    """Sequences with no query this step produce nothing; rows past the last
+    sequence's queries are left untouched."""
+    b = make_batch([40, 17, 90, 5], [1, 0, 3, 0], 8, 2, seed=9, device="cuda")
+    meta = to_device(b)
+    q = torch.cat([b.q, b.q[:2]])  # two trailing rows owned by nobody
+    out = torch.full_like(q, 7.0)
+    kc, vc = b.k_cache.clone(), b.v_cache.clone()
+    pkv.write(b.k_new, b.v_new, meta["slot_mapping"], kc, vc)
+    pkv.attend(q, kc, vc, meta["block_tables"], meta["seq_lens"], meta["query_start_loc"], b.scale, out=out)
+    torch.cuda.synchronize()
+    k_ref, v_ref = oracle_write(b)
+    expected = oracle_attend(b, k_ref, v_ref)
+    compare(out[: b.T], expected, what="zero-length")
+    assert torch.all(out[b.T:] == 7.0)
+
+
+def test_stale_nan_rows_do_not_leak(pkvlib):
+    """Rows of a sequence's last page beyond its length hold NaN; they must
+    not reach the output."""
+    b = make_batch([17, 33, 250, 64], [1, 4, 1, 20], 8, 2, seed=10, device="cuda")
+    kc, vc = b.k_cache, b.v_cache
+    for bi in range(b.B):
+        L = int(b.seq_lens[bi])
+        last = int(b.block_tables[bi, (L - 1) // 16])
+        if L % 16:
+            kc[last, :, L % 16:, :] = float("nan")
+            vc[last, :, L % 16:, :] = float("inf")
+    check_batch(b, what="nan-stale")
+
+
+def test_prefix_shared_identical_suffix_rows_agree(pkvlib):
+    """Two sequences sharing prefix pages and with identical suffix content
+    and query give identical outputs."""
+    b = make_batch([2048 + 40, 2048 + 40, 2048 + 77], [1, 1, 1], 32, 8, seed=11, device="cuda",
+                   pool_factor=1.0, shared_prefix_tokens=2048)
+    bt = b.block_tables
+    for j in range(128, 131):  # copy seq 0's suffix pages into seq 1's
+        b.k_cache[int(bt[1, j])] = b.k_cache[int(bt[0, j])]
+        b.v_cache[int(bt[1, j])] = b.v_cache[int(bt[0, j])]
+    b.k_new[1] = b.k_new[0]
+    b.v_new[1] = b.v_new[0]
+    b.q[1] = b.q[0]
+    out, _, _ = run_step(b)
+    assert torch.equal(out[0], out[1])
+    check_batch(b, what="prefix")
+
+
+def test_bad_block_id_is_flagged_not_read(pkvlib):
+    b = make_batch([100, 40], [1, 1], 8, 2, seed=12, device="cuda")
+    meta = to_device(b)
+    meta["block_tables"][0, 2] = b.num_blocks + 1000  # live entry out of the pool
+    pkv.get_last_error()
+    run_step(b, meta)
+    assert pkv.get_last_error() & pkv.STATUS_BAD_BLOCK
+
+
+def test_query_longer_than_sequence_is_flagged(pkvlib):
+    b = make_batch([10, 40], [1, 1], 8, 2, seed=13, device="cuda")
+    meta = to_device(b)
+    meta["seq_lens"][0] = 0  # 1 query row but 0 tokens
+    pkv.get_last_error()
+    run_step(b, meta)
+    assert pkv.get_last_error() & pkv.STATUS_BAD_QUERY
+
+
+def test_repeated_calls_reuse_workspace(pkvlib):
+    b = workload(2, device="cuda")
+    meta = to_device(b)
+    kc, vc = b.k_cache.clone(), b.v_cache.clone()
+    pkv.write(b.k_new, b.v_new, meta["slot_mapping"], kc, vc)
+    ws = torch.empty(pkv.workspace_size(pkv.make_desc(kc, b.num_q_heads, b.block_tables.shape[1]),
+                                        b.B, b.T), dtype=torch.uint8, device="cuda")
+    outs = [pkv.attend(b.q, kc, vc, meta["block_tables"], meta["seq_lens"], meta["query_start_loc"],
+                       b.scale, workspace=ws) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
