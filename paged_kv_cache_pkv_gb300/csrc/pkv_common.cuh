@@ -26,7 +26,7 @@ __host__ __device__ constexpr int partial_floats(int gh) { return kPartialHeader
 
 // Bounded waits: after this many failed mbarrier polls a kernel gives up,
 // flags PKV_STATUS_TIMEOUT and returns.
-constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr uint32_t kWaitLimit = 1u << 22;
 
 // Work plan written by the plan kernel into the caller's workspace.
 struct PlanHeader {
