@@ -73,6 +73,7 @@ typedef struct CUevent_st* pkv_event_t;    /* same handle as cudaEvent_t    */
 #define PKV_ERR_LAUNCH     (-6)  /* a CUDA launch or runtime call failed         */
 #define PKV_ERR_DEVICE     (-7)  /* current device is not an sm_103 GPU          */
 #define PKV_ERR_STATE      (-8)  /* misuse of the trace API                      */
+#define PKV_ERR_SCRATCH    (-9)  /* batch too large for pkv_attend_static        */
 
 /* ---- device status bits (pkv_get_last_error) ------------------------------- */
 #define PKV_STATUS_BAD_SLOT   0x1u  /* slot_mapping entry beyond the pool: skipped */
@@ -142,6 +143,36 @@ PKV_API int pkv_attend(const pkv_bf16* q, const pkv_bf16* k_cache,
                int32_t num_seqs, int32_t num_tokens, float scale,
                pkv_bf16* out, void* workspace, size_t workspace_bytes,
                const pkv_desc* desc, pkv_stream_t stream);
+
+/* pkv_attend_static -- pkv_attend for callers that cannot allocate device
+ * memory.  The pages this library follows have no counterpart for this call;
+ * it exists for users, not for the method.
+ *
+ * Who needs it: code that runs inside a host program which owns every byte
+ * of device memory and forbids allocation once it has started (fixed memory
+ * budgets decided at start-up), or a caller that reaches this library
+ * through a plain C interface and only ever holds pointers handed to it,
+ * with no device allocator of its own to size and create a workspace.
+ *
+ * Same arguments and results as pkv_attend, minus the workspace: the scratch
+ * memory lives in a fixed array of PKV_STATIC_SCRATCH_BYTES bytes inside the
+ * library, one per GPU that loads it, held until the process exits.  The
+ * call allocates nothing, on the device or through any library.
+ *   - Batches whose pkv_attend_workspace_size exceeds PKV_STATIC_SCRATCH_BYTES
+ *     are rejected with PKV_ERR_SCRATCH before anything is launched.
+ *   - The first call on each device looks up that device's copy of the array
+ *     (with the device current); make that first call before any stream
+ *     capture on the device.
+ *   - All calls on a device share the one array and it keeps what the last
+ *     call left there; the kernels need none of it cleared first.  Calls
+ *     whose work overlaps on the GPU (different streams, no ordering between
+ *     them) race on the array and give undefined results: serialise them. */
+#define PKV_STATIC_SCRATCH_BYTES (8u << 20)
+PKV_API int pkv_attend_static(const pkv_bf16* q, const pkv_bf16* k_cache,
+                              const pkv_bf16* v_cache, const int32_t* block_tables,
+                              const int32_t* seq_lens, const int32_t* query_start_loc,
+                              int32_t num_seqs, int32_t num_tokens, float scale,
+                              pkv_bf16* out, const pkv_desc* desc, pkv_stream_t stream);
 
 /* Wait for `stream`, then read and clear the current device's status word
  * (PKV_STATUS_* bits) into *flags. */

@@ -53,6 +53,8 @@ _SIGS = {
     "pkv_attend_workspace_size": (ctypes.c_int, [ctypes.POINTER(Desc), _i32, _i32, ctypes.POINTER(_sz)]),
     "pkv_attend": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, _vp, _vp,
                                   _sz, ctypes.POINTER(Desc), _vp]),
+    "pkv_attend_static": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, _vp,
+                                         ctypes.POINTER(Desc), _vp]),
     "pkv_get_last_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
     "pkv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_launch_count": (ctypes.c_uint64, []),

@@ -222,6 +222,7 @@ const char* pkv_strerror(int code) {
     case PKV_ERR_LAUNCH: return "a CUDA launch or runtime call failed";
     case PKV_ERR_DEVICE: return "the current device is not an sm_103 (GB300) GPU";
     case PKV_ERR_STATE: return "trace API misuse";
+    case PKV_ERR_SCRATCH: return "batch needs more scratch than PKV_STATIC_SCRATCH_BYTES (use pkv_attend with a workspace)";
     default: return "unknown error";
   }
 }
