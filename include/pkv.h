@@ -112,6 +112,9 @@ PKV_API int pkv_write(const pkv_bf16* k_new, const pkv_bf16* v_new,
               pkv_bf16* k_cache, pkv_bf16* v_cache,
               const pkv_desc* desc, pkv_stream_t stream);
 
+/* Most sequences a single pkv_attend call accepts (PKV_ERR_RANGE above). */
+#define PKV_MAX_SEQS 2048
+
 /* Workspace bytes pkv_attend needs on the CURRENT device for a batch of up
  * to num_seqs sequences and num_tokens query rows.  Writes *bytes. */
 PKV_API int pkv_attend_workspace_size(const pkv_desc* desc, int32_t num_seqs,

@@ -34,15 +34,17 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose=False, force=False, extra_flags=()):
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(verbose=False, force=False, extra_flags=(), lib_path=LIB, obj_dir=OUT_DIR):
+    """Compile the sources into ``lib_path``; ``extra_flags`` (e.g. -D tuning
+    macros) go to every nvcc call and need their own ``obj_dir``."""
+    os.makedirs(obj_dir, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(os.path.dirname(HERE), "include", "pkv.h"))
     nvcc = _nvcc()
 
     def compile_one(src):
         s = os.path.join(CSRC, src)
-        o = os.path.join(OUT_DIR, src + ".o")
+        o = os.path.join(obj_dir, src + ".o")
         if force or _stale(o, [s] + headers):
             cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-c", s, "-o", o]
             r = subprocess.run(cmd, capture_output=True, text=True)
@@ -54,13 +56,13 @@ def build(verbose=False, force=False, extra_flags=()):
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    if force or _stale(LIB, objs):
-        cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", *objs, "-o", LIB + ".tmp"]
+    if force or _stale(lib_path, objs):
+        cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", *objs, "-o", lib_path + ".tmp"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(LIB + ".tmp", LIB)
-    return LIB
+        os.replace(lib_path + ".tmp", lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

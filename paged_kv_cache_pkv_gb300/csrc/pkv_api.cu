@@ -70,17 +70,10 @@ const DeviceInfo* current_device(int* err) {
   fresh.cc_major = prop.major;
   fresh.cc_minor = prop.minor;
   fresh.smem_optin = prop.sharedMemPerBlockOptin;
-  int ctas = decode_ctas_per_sm(4);
-  for (int gh : {1, 2}) {
-    const int c = decode_ctas_per_sm(gh);
-    if (c > 0 && c < ctas) ctas = c;
-  }
-  if (ctas <= 0) {
-    *err = PKV_ERR_LAUNCH;
-    return nullptr;
-  }
-  fresh.dec_ctas_per_sm = ctas;
-  fresh.dec_warps_total = fresh.sm_count * ctas * kDecWarps;
+  // A variant that cannot be resident gets 0 warps; pkv_attend then rejects
+  // the head ratios that need it instead of failing here.
+  for (int v = 0; v < 3; ++v)
+    fresh.dec_warps[v] = fresh.sm_count * decode_ctas_per_sm(v) * kDecWarps;
   void* addr = nullptr;
   if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) {
     *err = PKV_ERR_LAUNCH;

@@ -16,47 +16,51 @@ constexpr int kPage = 16;       // tokens per page
 constexpr int kPageBytes = kPage * kHeadDim * 2;  // one (page, kv head): 4 KiB
 
 // Split-KV decode kernel shape.
-constexpr int kDecWarps = 4;     // independent worker warps per CTA
-constexpr int kDecStages = 3;    // pages (K+V) in flight per warp
-constexpr int kMaxGroupPerItem = 4;  // query heads handled per decode item
+#ifndef PKV_DEC_WARPS
+#define PKV_DEC_WARPS 8
+#endif
+#ifndef PKV_DEC_STAGES
+#define PKV_DEC_STAGES 3
+#endif
+#ifndef PKV_DEC_MIN_CTAS
+#define PKV_DEC_MIN_CTAS 1
+#endif
+constexpr int kDecWarps = PKV_DEC_WARPS;    // warps per CTA
+constexpr int kDecStages = PKV_DEC_STAGES;  // pages (K+V) in flight per warp
+constexpr int kMaxGroupPerItem = 4;  // query heads sharing one page read
 
-// A decode partial state: m[4], l[4], then o[GH][128] (fp32).
+// A decode partial state of one warp: m[4], l[4], then o[heads][128] (fp32).
 constexpr int kPartialHeader = 8;
-__host__ __device__ constexpr int partial_floats(int gh) { return kPartialHeader + gh * kHeadDim; }
+__host__ __device__ constexpr int partial_floats(int heads) {
+  return kPartialHeader + heads * kHeadDim;
+}
 
 // Bounded waits: after this many failed mbarrier polls a kernel gives up,
 // flags PKV_STATUS_TIMEOUT and returns.
 constexpr uint32_t kWaitLimit = 1u << 22;
 
-// Work plan written by the plan kernel into the caller's workspace.
-struct PlanHeader {
-  int32_t units;   // total (row, kv head group, page) units of the split-KV path
-  int32_t chunk;   // units per decode warp
-  int32_t nwarps;  // decode warps the plan was made for
-  int32_t prefill_tiles;  // tensor-core prefill tiles in the tile list
-};
+// Most sequences one pkv_attend call may carry (the per-sequence unit prefix
+// of the split-KV plan lives in shared memory).
+constexpr int kMaxSeqs = 2048;
 
 // Workspace carve-up; every piece starts 256-byte aligned.
 struct WorkspaceLayout {
-  size_t header, row_unit_start, row_seq, row_nvis, warp_first_row, tiles, partials, total;
+  size_t counters, partials, tiles, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline WorkspaceLayout workspace_layout(int num_seqs, int num_tokens, int nwarps, int gh,
-                                        int max_tiles) {
+// counters_per_row: arrival counters per query row (items x warps per ring);
+// heads_per_warp sizes one partial slot; every decode warp owns two slots.
+inline WorkspaceLayout workspace_layout(int num_tokens, int counters_per_row, int nwarps,
+                                        int heads_per_warp, int max_tiles) {
   WorkspaceLayout w{};
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t at = off; off = align_up(off + bytes, 256); return at; };
-  w.header = take(sizeof(PlanHeader));
-  w.row_unit_start = take(sizeof(int32_t) * (size_t(num_tokens) + 1));
-  w.row_seq = take(sizeof(int32_t) * size_t(num_tokens));
-  w.row_nvis = take(sizeof(int32_t) * size_t(num_tokens));
-  w.warp_first_row = take(sizeof(int32_t) * size_t(nwarps));
-  w.tiles = take(sizeof(int32_t) * 2 * size_t(max_tiles));
-  w.partials = take(sizeof(float) * size_t(partial_floats(gh)) * 2 * size_t(nwarps));
+  w.counters = take(sizeof(unsigned long long) * size_t(num_tokens) * size_t(counters_per_row));
+  w.partials = take(sizeof(float) * size_t(partial_floats(heads_per_warp)) * 2 * size_t(nwarps));
+  w.tiles = take(sizeof(int32_t) * 4 * size_t(max_tiles));
   w.total = off;
-  (void)num_seqs;
   return w;
 }
 

@@ -13,8 +13,9 @@ struct DeviceInfo {
   int device = -1;
   int sm_count = 0;
   int cc_major = 0, cc_minor = 0;
-  int dec_ctas_per_sm = 0;   // resident split-KV decode CTAs per SM
-  int dec_warps_total = 0;   // decode warps of one persistent launch
+  // Decode warps of one persistent launch, per kernel variant: index 0, 1, 2
+  // for 1, 2, 4 query heads sharing a page read.
+  int dec_warps[3] = {0, 0, 0};
   size_t smem_optin = 0;
 };
 
@@ -66,12 +67,14 @@ size_t attend_workspace_bytes(const DeviceInfo& dev, const pkv_desc& d, int32_t 
                               int32_t num_tokens);
 int launch_attend(const LaunchCtx& ctx, const AttendArgs& a);
 
-// Resident CTAs per SM of the decode kernel (occupancy query).
-int decode_ctas_per_sm(int group_per_item);
+// Resident CTAs per SM of the decode kernel variant (occupancy query).
+int decode_ctas_per_sm(int variant);
 
 // Tensor-core chunked-prefill path (pkv_prefill.cu).
 int prefill_max_tiles(const pkv_desc& d, int32_t num_seqs, int32_t num_tokens);
-int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, const void* tiles,
-                   const void* header, int max_tiles);
+// Launches the prefill kernel for sequences with more than split_max_q query
+// rows; `scratch` is the workspace's tile area.
+int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, void* scratch, int split_max_q,
+                   int max_tiles);
 
 }  // namespace pkv

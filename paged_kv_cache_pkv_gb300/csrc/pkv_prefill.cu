@@ -7,7 +7,7 @@ namespace pkv {
 
 int prefill_max_tiles(const pkv_desc&, int32_t, int32_t) { return 0; }
 
-int launch_prefill(const LaunchCtx&, const AttendArgs&, const void*, const void*, int) {
+int launch_prefill(const LaunchCtx&, const AttendArgs&, void*, int, int) {
   return PKV_OK;
 }
 

@@ -22,6 +22,9 @@ __global__ void __launch_bounds__(256) pkv_write_kernel(
     const int64_t* __restrict__ slot_mapping, int64_t num_tokens, uint4* __restrict__ k_cache,
     uint4* __restrict__ v_cache, int32_t num_blocks, int32_t num_kv_heads,
     unsigned* __restrict__ status) {
+  // Let a dependent attention kernel start its set-up now; it waits for this
+  // grid's writes before it reads the pool.
+  asm volatile("griddepcontrol.launch_dependents;");
   constexpr int kVecPerRow = kHeadDim * 2 / 16;  // 16 vectors of 16 B per row
   const int64_t rows = num_tokens * num_kv_heads;
   const int64_t total = rows * 2 * kVecPerRow;   // K and V
