@@ -225,9 +225,11 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    max_q = int(b.q_lens.max())  # the scheduler knows its largest query chunk
+
     def step():
         pkv.write(b.k_new, b.v_new, slots, kc, vc)
-        pkv.attend(b.q, kc, vc, bt, lens, qsl, b.scale, out=out, workspace=ws)
+        pkv.attend(b.q, kc, vc, bt, lens, qsl, b.scale, out=out, workspace=ws, max_query_len=max_q)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -312,7 +314,7 @@ def main():
             dev_in[name].copy_(x, non_blocking=True)
         pkv.write(dev_in["k_new"], dev_in["v_new"], dev_in["slots"], kc, vc)
         pkv.attend(dev_in["q"], kc, vc, dev_in["bt"], dev_in["lens"], dev_in["qsl"], b.scale, out=out,
-                   workspace=ws)
+                   workspace=ws, max_query_len=max_q)
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(3):

@@ -114,6 +114,9 @@ PKV_API int pkv_write(const pkv_bf16* k_new, const pkv_bf16* v_new,
 
 /* Most sequences a single pkv_attend call accepts (PKV_ERR_RANGE above). */
 #define PKV_MAX_SEQS 2048
+/* Sequences with more query rows than this use the tensor-core prefill
+ * kernel (the environment variable PKV_SPLITKV_MAX_QLEN overrides it). */
+#define PKV_SPLITKV_MAX_QLEN 8
 
 /* Workspace bytes pkv_attend needs on the CURRENT device for a batch of up
  * to num_seqs sequences and num_tokens query rows.  Writes *bytes. */
@@ -134,6 +137,13 @@ PKV_API int pkv_attend_workspace_size(const pkv_desc* desc, int32_t num_seqs,
  *                 n_b <= L_b).  Row j of b is at position L_b-n_b+j and sees
  *                 keys 0..L_b-n_b+j (bottom-right causal; n_b == 1 is
  *                 decode over all L_b keys).
+ *   max_query_len host-side upper bound on n_b over the batch, or <= 0 if
+ *                 unknown.  It only selects kernels: sequences with more
+ *                 than PKV_SPLITKV_MAX_QLEN query rows run on the tensor-core
+ *                 prefill kernel, the rest on split-KV; when the bound is at
+ *                 most that threshold the prefill kernel is not launched and
+ *                 split-KV takes every row, so a wrong bound never changes
+ *                 results.
  *   scale         softmax scale applied to q.k (e.g. 1/sqrt(head_dim)).
  *   out           [num_tokens, num_q_heads, head_dim] bf16, device; rows at
  *                 or beyond query_start_loc[num_seqs] are not written.
@@ -143,9 +153,10 @@ PKV_API int pkv_attend_workspace_size(const pkv_desc* desc, int32_t num_seqs,
 PKV_API int pkv_attend(const pkv_bf16* q, const pkv_bf16* k_cache,
                const pkv_bf16* v_cache, const int32_t* block_tables,
                const int32_t* seq_lens, const int32_t* query_start_loc,
-               int32_t num_seqs, int32_t num_tokens, float scale,
-               pkv_bf16* out, void* workspace, size_t workspace_bytes,
-               const pkv_desc* desc, pkv_stream_t stream);
+               int32_t num_seqs, int32_t num_tokens, int32_t max_query_len,
+               float scale, pkv_bf16* out, void* workspace,
+               size_t workspace_bytes, const pkv_desc* desc,
+               pkv_stream_t stream);
 
 /* pkv_attend_static -- pkv_attend for callers that cannot allocate device
  * memory.  The pages this library follows have no counterpart for this call;
@@ -174,8 +185,9 @@ PKV_API int pkv_attend(const pkv_bf16* q, const pkv_bf16* k_cache,
 PKV_API int pkv_attend_static(const pkv_bf16* q, const pkv_bf16* k_cache,
                               const pkv_bf16* v_cache, const int32_t* block_tables,
                               const int32_t* seq_lens, const int32_t* query_start_loc,
-                              int32_t num_seqs, int32_t num_tokens, float scale,
-                              pkv_bf16* out, const pkv_desc* desc, pkv_stream_t stream);
+                              int32_t num_seqs, int32_t num_tokens,
+                              int32_t max_query_len, float scale, pkv_bf16* out,
+                              const pkv_desc* desc, pkv_stream_t stream);
 
 /* Wait for `stream`, then read and clear the current device's status word
  * (PKV_STATUS_* bits) into *flags. */

@@ -51,10 +51,10 @@ _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c
 _SIGS = {
     "pkv_write": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp, _vp, ctypes.POINTER(Desc), _vp]),
     "pkv_attend_workspace_size": (ctypes.c_int, [ctypes.POINTER(Desc), _i32, _i32, ctypes.POINTER(_sz)]),
-    "pkv_attend": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, _vp, _vp,
-                                  _sz, ctypes.POINTER(Desc), _vp]),
-    "pkv_attend_static": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, _vp,
-                                         ctypes.POINTER(Desc), _vp]),
+    "pkv_attend": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_float, _vp,
+                                  _vp, _sz, ctypes.POINTER(Desc), _vp]),
+    "pkv_attend_static": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_float,
+                                         _vp, ctypes.POINTER(Desc), _vp]),
     "pkv_get_last_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
     "pkv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_launch_count": (ctypes.c_uint64, []),
@@ -144,11 +144,13 @@ def workspace_size(desc, num_seqs, num_tokens, device=None):
 
 
 def attend(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, out=None,
-           workspace=None, stream=None):
+           workspace=None, stream=None, max_query_len=0):
     """Paged GQA attention of one continuous batch; returns ``out`` [T, Hq, D].
 
     ``workspace`` (uint8 CUDA tensor) may be passed to avoid an allocation by
-    PyTorch's caching allocator on every call."""
+    PyTorch's caching allocator on every call.  ``max_query_len`` is an
+    optional host-side upper bound on query rows per sequence (0 = unknown);
+    it only selects kernels, never results."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_cache, "k_cache", torch.bfloat16, 4)
     _need(v_cache, "v_cache", torch.bfloat16, 4)
@@ -177,8 +179,9 @@ def attend(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, 
             raise ValueError(f"workspace needs {need} bytes, got {workspace.numel()}")
     with torch.cuda.device(q.device):
         _check(lib().pkv_attend(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens),
-                                _ptr(query_start_loc), B, T, float(scale), _ptr(out), _ptr(workspace),
-                                workspace.numel(), ctypes.byref(desc), _stream(q.device, stream)),
+                                _ptr(query_start_loc), B, T, int(max_query_len), float(scale), _ptr(out),
+                                _ptr(workspace), workspace.numel(), ctypes.byref(desc),
+                                _stream(q.device, stream)),
                "pkv_attend")
     return out
 

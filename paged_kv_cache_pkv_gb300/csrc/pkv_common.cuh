@@ -35,9 +35,10 @@ __host__ __device__ constexpr int partial_floats(int heads) {
   return kPartialHeader + heads * kHeadDim;
 }
 
-// Bounded waits: after this many failed mbarrier polls a kernel gives up,
-// flags PKV_STATUS_TIMEOUT and returns.
-constexpr uint32_t kWaitLimit = 1u << 22;
+// Bounded waits: a kernel gives up on an mbarrier after this many
+// nanoseconds of polling, flags PKV_STATUS_TIMEOUT and returns.
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // 200 ms
+constexpr uint64_t kDrainLimitNs = 2ull * 1000 * 1000;   // 2 ms for the clean-up path
 
 // Most sequences one pkv_attend call may carry (the per-sequence unit prefix
 // of the split-KV plan lives in shared memory).
@@ -104,12 +105,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Wait for the phase with the given parity; false if the bound ran out.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase with the given parity; false once limit_ns have passed.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          uint32_t limit = kWaitLimit) {
-  for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
+                                          uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > limit_ns) return false;
+  return true;
 }
 
 // L2 policy for data read exactly once (KV pages of a decode step).

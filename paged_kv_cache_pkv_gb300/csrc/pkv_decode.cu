@@ -645,7 +645,7 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
     if (lane == 0) flag_status(p.status, PKV_STATUS_TIMEOUT);
     // let copies still in flight land before the CTA's shared memory is released
     for (int k = it; k < min(n_units, it + kDecStages); ++k)
-      mbar_wait(&R.bar[k % kDecStages], (k / kDecStages) & 1, 1u << 16);
+      mbar_wait(&R.bar[k % kDecStages], (k / kDecStages) & 1, kDrainLimitNs);
     return;
   }
   if (cur_row >= 0) flush_segment();
@@ -692,7 +692,7 @@ int decode_ctas_per_sm(int variant) {
 static int simt_max_q() {
   static int v = [] {
     const char* e = getenv("PKV_SPLITKV_MAX_QLEN");
-    return e ? atoi(e) : 8;
+    return e ? atoi(e) : PKV_SPLITKV_MAX_QLEN;
   }();
   return v;
 }
@@ -751,9 +751,12 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   if (a.workspace_bytes < L.total) return PKV_ERR_WORKSPACE;
   if (a.num_tokens == 0 || a.num_seqs == 0) return PKV_OK;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  const int split_max_q = max_tiles > 0 ? simt_max_q() : INT_MAX;
-
-  if (max_tiles > 0) {
+  // Long query chunks go to the tensor-core kernel unless the caller's bound
+  // says there are none; then split-KV takes every row.
+  const bool prefill = max_tiles > 0 && a.num_tokens > simt_max_q() &&
+                       (a.max_query_len <= 0 || a.max_query_len > simt_max_q());
+  const int split_max_q = prefill ? simt_max_q() : INT_MAX;
+  if (prefill) {
     if (int e = launch_prefill(ctx, a, ws + L.tiles, split_max_q, max_tiles)) return e;
   }
 

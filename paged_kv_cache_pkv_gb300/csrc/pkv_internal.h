@@ -54,7 +54,7 @@ struct AttendArgs {
   const int32_t* block_tables;
   const int32_t* seq_lens;
   const int32_t* query_start_loc;
-  int32_t num_seqs, num_tokens;
+  int32_t num_seqs, num_tokens, max_query_len;
   float scale;
   uint16_t* out;
   void* workspace;

@@ -1,14 +1,633 @@
-// pkv_prefill.cu -- tensor-core path for chunked-prefill query rows.
-// (Until this kernel is enabled every query row goes through split-KV.)
+// pkv_prefill.cu -- chunked-prefill attention on the 5th-generation tensor
+// cores (tcgen05 + TMEM + TMA) for sequences with many query rows.
+//
+// What is computed (llm-d blog post "What does production-grade LLM inference
+// look like?", introduction: prefill is compute bound; with continuous
+// batching a step carries prefill chunks next to decode rows): for query j of
+// a chunk of n tokens in a sequence of L cached tokens, softmax attention over
+// keys 0 .. L-n+j (bottom-right causal), query head h reading kv head h/G.
+//
+// Design (GB300):
+//  * One CTA = one tile of 128 query rows: TM = 128/G query tokens x the G
+//    query heads of one kv head (row = token*G + head), so every K/V tile
+//    loaded serves all G heads of the group.
+//  * Q tile: two TMA boxes (64 dims each, 128-byte swizzle) from q viewed as
+//    [T][Hq][128].  K and V tiles of 128 keys = 8 pages, each page two TMA
+//    boxes of 16 rows x 64 dims from the pool viewed as [NB*Hkv*16][128];
+//    page ids come from the block table, pages past the sequence are skipped.
+//    K/V tiles are double-buffered: tile i+1 loads while tile i computes.
+//  * S = Q K^T: 8 tcgen05.mma (M=128, N=128, K=16, bf16 in, fp32 out) into
+//    TMEM columns 0..127; both operands K-major in shared memory.
+//  * Softmax: threads t and t+128 own TMEM lane t%128 (query row t%128), 64
+//    score columns each: tcgen05.ld, bottom-right causal mask, exp2 against
+//    the running max in the log2 domain, row max exchanged through shared
+//    memory.  The running max only moves when a score exceeds it by more than
+//    kTau (then the pass is redone and O in TMEM is rescaled), so most tiles
+//    take one pass.  P is rounded to bf16 into shared memory in the same
+//    swizzled K-major layout.
+//  * O += P V: 8 tcgen05.mma into TMEM columns 128..255; V is the N-major
+//    (dims contiguous) operand.  V rows past the sequence end are zeroed in
+//    shared memory first so stale pool contents cannot reach O.
+//  * Warp roles: warps 0-7 run the softmax; warp 8 (one lane) issues every TMA
+//    copy and tcgen05.mma, so block-table loads and copy issue never sit on
+//    the softmax's path.  Softmax -> MMA hand-off is an mbarrier ("P ready",
+//    256 arrivals); MMA -> softmax is tcgen05.commit on "S ready" / "O done".
+//  * Every mbarrier wait is bounded; on expiry the CTA flags
+//    PKV_STATUS_TIMEOUT, lets its in-flight copies and MMAs land, frees TMEM
+//    and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <mutex>
+#include <type_traits>
+
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
 
-int prefill_max_tiles(const pkv_desc&, int32_t, int32_t) { return 0; }
+constexpr int kPfSoftmaxThreads = 256;  // two threads per query row (64 score columns each)
+constexpr int kPfThreads = kPfSoftmaxThreads + 32;  // + one warp issuing TMA and MMA
+constexpr int kPfKeys = 128;          // keys per K/V tile (8 pages)
+constexpr int kPfPagesPerTile = kPfKeys / kPage;
+constexpr uint32_t kTmemCols = 256;   // S: [0,128), O: [128,256)
+constexpr float kPfTau = 8.0f;
 
-int launch_prefill(const LaunchCtx&, const AttendArgs&, void*, int, int) {
-  return PKV_OK;
+// Shared-memory map (offsets from a 1024-byte aligned base).
+constexpr uint32_t kHalfTile = 128 * 128;          // 128 rows x 64 bf16 = 16 KiB
+constexpr uint32_t kOffQ = 0;                      // [2 halves]
+constexpr uint32_t kOffK = kOffQ + 2 * kHalfTile;  // [2 bufs][2 halves]
+constexpr uint32_t kOffV = kOffK + 4 * kHalfTile;  // [2 bufs][2 halves]
+constexpr uint32_t kOffP = kOffV + 4 * kHalfTile;  // [2 halves]
+constexpr uint32_t kOffMisc = kOffP + 2 * kHalfTile;
+constexpr uint32_t kPfSmemBytes = kOffMisc + 2048 + 1024;  // + misc (barriers, row exchange) + alignment slack
+
+struct PrefillParams {
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  uint16_t* out;
+  unsigned* status;
+  int32_t B, T, Hkv, Hq, G, TM, max_blocks, num_blocks, split_max_q;
+  float qscale;  // scale * log2(e)
+};
+
+// ---------------------------------------------------------------------------
+// tcgen05 / TMA helpers
+// ---------------------------------------------------------------------------
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
+// address, leading and stride byte offsets in 16-byte units, version 1).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(b_mn_major) << 16) |
+         (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31]));
+}
+
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Barrier over `threads` threads that also ORs a per-thread flag: every
+// participant gets the same result.
+__device__ __forceinline__ bool named_sync_or(int id, int threads, bool flag) {
+  uint32_t res;
+  asm volatile(
+      "{\n\t.reg .pred pin, pout;\n\t"
+      "setp.ne.u32 pin, %1, 0;\n\t"
+      "bar.red.or.pred pout, %2, %3, pin;\n\t"
+      "selp.u32 %0, 1, 0, pout;\n\t}"
+      : "=r"(res)
+      : "r"(uint32_t(flag)), "r"(id), "r"(threads)
+      : "memory");
+  return res != 0;
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kPfThreads, 1)
+    pkv_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = sm + kOffQ;
+  uint8_t* sK = sm + kOffK;
+  uint8_t* sV = sm + kOffV;
+  uint8_t* sP = sm + kOffP;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffMisc);  // q, kv0, kv1, s, o, p
+  uint64_t* bar_q = bars;
+  uint64_t* bar_kv = bars + 1;
+  uint64_t* bar_s = bars + 3;
+  uint64_t* bar_o = bars + 4;
+  uint64_t* bar_p = bars + 5;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 64);
+  int* s_info = reinterpret_cast<int*>(sm + kOffMisc + 72);  // b, t0, total tiles
+  int* s_scan = reinterpret_cast<int*>(sP);  // plan scratch, reused by P later
+  __shared__ int s_wsum[kPfThreads / 32];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = blockIdx.x;  // kv head; blockIdx.y = tile (real tiles dispatch first)
+
+  // ---- plan: which (sequence, first query token) this CTA's tile is --------
+  {
+    const int per = (p.B + kPfThreads - 1) / kPfThreads;
+    const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
+    int local = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int q0 = __ldg(p.qsl + b), q1 = __ldg(p.qsl + b + 1), L = __ldg(p.seq_lens + b);
+      const int n = q1 - q0;
+      const bool bad = q0 < 0 || n < 0 || q1 > p.T || n > L || L < 0 ||
+                       (L + kPage - 1) / kPage > p.max_blocks || (b == 0 && q0 != 0);
+      const int tiles = (!bad && n > p.split_max_q) ? (n + p.TM - 1) / p.TM : 0;
+      s_scan[b] = tiles;
+      local += tiles;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    int base = 0, total = 0;
+#pragma unroll
+    for (int x = 0; x < kPfThreads / 32; ++x) {
+      if (x < warp) base += s_wsum[x];
+      total += s_wsum[x];
+    }
+    int run = base + incl - local;
+    for (int b = b0; b < b1; ++b) {
+      const int c = s_scan[b];
+      s_scan[b] = run;
+      run += c;
+    }
+    if (tid == 0) s_scan[p.B] = total;
+    __syncthreads();
+    if (tid == 0) {
+      // heavier tiles (later sequences, later query blocks) first
+      const int i = total - 1 - int(blockIdx.y);
+      int b = -1, t0 = 0;
+      if (i >= 0) {
+        int lo = 0, hi = p.B;  // last b with s_scan[b] <= i
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (s_scan[mid] <= i) lo = mid; else hi = mid;
+        }
+        b = lo;
+        t0 = (i - s_scan[lo]) * p.TM;
+      }
+      s_info[0] = b;
+      s_info[1] = t0;
+    }
+    __syncthreads();
+  }
+  const int b = s_info[0];
+  if (b < 0) return;  // no tile for this CTA (before any TMEM is taken)
+  const int t0 = s_info[1];
+  const int q0 = __ldg(p.qsl + b);
+  const int n = __ldg(p.qsl + b + 1) - q0;
+  const int L = __ldg(p.seq_lens + b);
+  const int npages = (L + kPage - 1) / kPage;
+  const int max_pos = L - n + min(n, t0 + p.TM) - 1;
+  const int nkv = max_pos / kPfKeys + 1;
+
+  // ---- barriers and TMEM -----------------------------------------------------
+  if (tid == 0) {
+    for (int i = 0; i < 5; ++i) mbar_init(bars + i, 1);
+    mbar_init(bar_p, kPfSoftmaxThreads);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(s_tmem)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t tmem_s = tmem, tmem_o = tmem + 128;
+  const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;  // warp w reads TMEM lanes 32*(w%4)..
+
+  // ---- producer helpers (thread 0) ---------------------------------------------
+  auto load_kv = [&](int kt, int buf) {
+    int valid = 0;
+    int bids[kPfPagesPerTile];
+#pragma unroll
+    for (int j = 0; j < kPfPagesPerTile; ++j) {
+      const int pi = kt * kPfPagesPerTile + j;
+      int bid = -1;
+      if (pi < npages) {
+        bid = __ldg(p.block_tables + int64_t(b) * p.max_blocks + pi);
+        if (bid < 0 || bid >= p.num_blocks) {
+          flag_status(p.status, PKV_STATUS_BAD_BLOCK);
+          bid = 0;
+        }
+        ++valid;
+      }
+      bids[j] = bid;
+    }
+    mbar_arrive_expect_tx(bar_kv + buf, uint32_t(valid) * 4 * 2048);
+#pragma unroll
+    for (int j = 0; j < kPfPagesPerTile; ++j) {
+      if (bids[j] < 0) continue;
+      const int row = (bids[j] * p.Hkv + g) * kPage;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        tma_load_2d(sK + (buf * 2 + h) * kHalfTile + j * 2048, &tm_k, h * 64, row, bar_kv + buf);
+        tma_load_2d(sV + (buf * 2 + h) * kHalfTile + j * 2048, &tm_v, h * 64, row, bar_kv + buf);
+      }
+    }
+  };
+
+  const uint32_t idesc_s = idesc_bf16(128, 128, false);
+  const uint32_t idesc_o = idesc_bf16(128, 128, true);
+  const bool mma_warp = warp == kPfSoftmaxThreads / 32;
+
+  if (mma_warp) {
+    // ===== TMA + MMA issuer (one lane) =====
+    if (lane == 0) {
+      int issued = 0, n_s = 0, n_pv = 0;
+      bool ok = true;
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+      mbar_arrive_expect_tx(bar_q, 2 * kHalfTile);
+      for (int h = 0; h < 2; ++h)
+        tma_load_3d(sQ + h * kHalfTile, &tm_q, h * 64, g * p.G, q0 + t0, bar_q);
+      for (; issued < min(2, nkv); ++issued) load_kv(issued, issued & 1);
+      auto issue_s = [&](int kt) {
+        const int buf = kt & 1;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const int h = ks >> 2, kk = ks & 3;
+          const uint64_t a = smem_desc(smem_u32(sQ + h * kHalfTile) + kk * 32, 16, 1024);
+          const uint64_t bdesc = smem_desc(smem_u32(sK + (buf * 2 + h) * kHalfTile) + kk * 32, 16, 1024);
+          umma(tmem_s, a, bdesc, idesc_s, ks > 0);
+        }
+        umma_commit(bar_s);
+        ++n_s;
+      };
+      ok = mbar_wait(bar_q, 0) && mbar_wait(bar_kv, 0);
+      if (ok) issue_s(0);
+      for (int it = 0; ok && it < nkv; ++it) {
+        const int buf = it & 1;
+        // P of tile it is in shared memory (and O rescaled if needed)
+        if (!(ok = mbar_wait(bar_p, it & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const int h = ks >> 2, kk = ks & 3;
+          const uint64_t a = smem_desc(smem_u32(sP + h * kHalfTile) + kk * 32, 16, 1024);
+          const uint64_t bdesc = smem_desc(smem_u32(sV + buf * 2 * kHalfTile) + ks * 2048, kHalfTile, 1024);
+          umma(tmem_o, a, bdesc, idesc_o, (it > 0 || ks > 0) ? 1u : 0u);
+        }
+        umma_commit(bar_o);
+        ++n_pv;
+        if (it + 1 < nkv) {
+          if (!(ok = mbar_wait(bar_kv + ((it + 1) & 1), ((it + 1) >> 1) & 1))) break;
+          issue_s(it + 1);
+        }
+        if (issued < nkv) {  // tile it's buffer frees once PV(it) is done
+          if (!(ok = mbar_wait(bar_o, it & 1))) break;
+          load_kv(issued, issued & 1);
+          ++issued;
+        }
+      }
+      if (!ok) {
+        flag_status(p.status, PKV_STATUS_TIMEOUT);
+        // Let what was issued land before TMEM and shared memory are released:
+        // the newest copy on each buffer and the newest commit of each kind
+        // (older phases completed before these were issued).
+        for (int k = max(0, issued - 2); k < issued; ++k)
+          mbar_wait(bar_kv + (k & 1), (k >> 1) & 1, kDrainLimitNs);
+        if (n_s > 0) mbar_wait(bar_s, (n_s - 1) & 1, kDrainLimitNs);
+        if (n_pv > 0) mbar_wait(bar_o, (n_pv - 1) & 1, kDrainLimitNs);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ===== softmax warps =====
+    const int r = tid & 127;  // query row == TMEM lane
+    const int ch = tid >> 7;  // which 64 of the 128 score columns
+    const int t_rel = r / p.G;
+    const bool row_valid = t0 + t_rel < n;
+    const int pos = row_valid ? L - n + t0 + t_rel : L - 1;
+    float m = -INFINITY, l = 0.f;  // running max (same in both threads of a row), half row sum
+    float* s_red = reinterpret_cast<float*>(sm + kOffMisc + 128);  // [2][128] exchange
+    bool ok = true;
+    for (int it = 0; it < nkv; ++it) {
+      const int buf = it & 1;
+      ok = mbar_wait(bar_s, it & 1);
+      if (it > 0) ok = ok && mbar_wait(bar_o, (it - 1) & 1);
+      tc_fence_after();
+      // ---- this thread's 64 columns of row r ----
+      const int kbase = it * kPfKeys + ch * 64;
+      // no masking in this half tile for any row of the warp: the pass below
+      // runs warp-collective TMEM loads, so the choice must be warp-uniform
+      const bool full = __all_sync(0xffffffffu, kbase + 63 <= pos);
+      const uint32_t scol = tmem_s + lane_off + ch * 64;
+      uint32_t pk[2][16];
+      float mx = -INFINITY, rs = 0.f;
+      // One pass over the 64 columns: exp2(s*scale - mref) packed to bf16,
+      // optionally tracking the raw maximum.  FULL: no key of this half tile
+      // is past the row's position (no masking work at all).
+      auto pass = [&](float mref, auto full_t, auto track_t) {
+        constexpr bool FULL = decltype(full_t)::value, TRACK = decltype(track_t)::value;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float mxl[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t sv[32];
+          tmem_ld32(scol + c * 32, sv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float x0 = __uint_as_float(sv[2 * e]), x1 = __uint_as_float(sv[2 * e + 1]);
+            if constexpr (!FULL) {
+              const int k = kbase + c * 32 + 2 * e;
+              if (k > pos) x0 = -INFINITY;
+              if (k + 1 > pos) x1 = -INFINITY;
+            }
+            if constexpr (TRACK) {
+              mxl[0] = fmaxf(mxl[0], x0);
+              mxl[1] = fmaxf(mxl[1], x1);
+            }
+            const float a0 = ex2(fmaf(x0, p.qscale, -mref));  // exp2(-inf) = 0
+            const float a1 = ex2(fmaf(x1, p.qscale, -mref));
+            acc[e & 3] += a0 + a1;
+            pk[c][e] = pack_bf16x2(a0, a1);
+          }
+        }
+        rs = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        if constexpr (TRACK) mx = fmaxf(mxl[0], mxl[1]);
+      };
+      if (full) pass(m, std::true_type{}, std::true_type{});
+      else pass(m, std::false_type{}, std::true_type{});
+      s_red[ch * 128 + r] = mx;
+      named_sync(1, kPfSoftmaxThreads);
+      const float row_mx = fmaxf(s_red[r], s_red[128 + r]) * p.qscale;
+      // s_red may be rewritten next tile; a failed wait anywhere stops every
+      // softmax thread here, together
+      if (named_sync_or(2, kPfSoftmaxThreads, !ok)) {
+        ok = false;
+        break;
+      }
+      const bool grow = row_mx > m + kPfTau;
+      float alpha = 1.f;
+      if (grow) {
+        alpha = m == -INFINITY ? 0.f : ex2(m - row_mx);
+        m = row_mx;
+      }
+      // redo the pass against the new maximum; warp-uniform (TMEM loads are
+      // warp-collective), rows whose maximum did not move recompute the same P
+      if (__any_sync(0xffffffffu, grow)) {
+        if (full) pass(m, std::true_type{}, std::false_type{});
+        else pass(m, std::false_type{}, std::false_type{});
+      }
+      l = l * alpha + rs;
+      uint8_t* prow = sP + r * 128;
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int chunk = c * 4 + q;  // 16-byte chunk of the 128-byte row in half ch
+          uint4* dst = reinterpret_cast<uint4*>(prow + ch * kHalfTile + ((chunk ^ (r & 7)) << 4));
+          *dst = make_uint4(pk[c][4 * q], pk[c][4 * q + 1], pk[c][4 * q + 2], pk[c][4 * q + 3]);
+        }
+      // rescale this thread's 64 O columns when the running max moved
+      if (it > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tmem_o + lane_off + ch * 64 + c * 32, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st32(tmem_o + lane_off + ch * 64 + c * 32, ov);
+        }
+        tmem_wait_st();
+      }
+      // keys past the sequence end: zero their V rows so stale data cannot leak
+      if (it * kPfKeys + r >= L) {
+        uint4* vrow = reinterpret_cast<uint4*>(sV + (buf * 2 + ch) * kHalfTile + r * 128);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) vrow[q] = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_p);  // P of this tile is ready for the MMA warp
+    }
+    // ---- epilogue: O / l -> bf16, each thread its 64 columns of row r ----
+    ok = ok && mbar_wait(bar_o, (nkv - 1) & 1);
+    s_red[ch * 128 + r] = l;
+    named_sync(1, kPfSoftmaxThreads);
+    tc_fence_after();
+    const float inv = 1.f / (s_red[r] + s_red[128 + r]);
+    uint16_t* orow = p.out + (size_t(q0 + t0 + t_rel) * p.Hq + g * p.G + (r % p.G)) * kHeadDim + ch * 64;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      uint32_t ov[32];
+      tmem_ld32(tmem_o + lane_off + ch * 64 + c * 32, ov);
+      tmem_wait_ld();
+      if (row_valid && ok) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w4[e] = pack_bf16x2(__uint_as_float(ov[8 * q + 2 * e]) * inv,
+                                __uint_as_float(ov[8 * q + 2 * e + 1]) * inv);
+          dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+      }
+    }
+    if (!ok && tid == 0) flag_status(p.status, PKV_STATUS_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Query tokens per tile: 128 rows / G heads.
+static int tile_tokens(const pkv_desc& d) { return 128 / (d.num_q_heads / d.num_kv_heads); }
+
+int prefill_max_tiles(const pkv_desc& d, int32_t num_seqs, int32_t num_tokens) {
+  // every sequence may end in a partial tile
+  const int tm = tile_tokens(d);
+  return (num_tokens + tm - 1) / tm + num_seqs;
+}
+
+int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, void* /*scratch*/, int split_max_q,
+                   int max_tiles) {
+  const pkv_desc& d = a.desc;
+  const int G = d.num_q_heads / d.num_kv_heads;
+  static bool attr_set[64] = {};
+  if (ctx.dev->device >= 0 && ctx.dev->device < 64 && !attr_set[ctx.dev->device]) {
+    if (cudaFuncSetAttribute(pkv_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kPfSmemBytes)) != cudaSuccess) {
+      cudaGetLastError();
+      return PKV_ERR_LAUNCH;
+    }
+    attr_set[ctx.dev->device] = true;
+  }
+  CUtensorMap tq, tk, tv;
+  {
+    const cuuint64_t dims[3] = {cuuint64_t(kHeadDim), cuuint64_t(d.num_q_heads), cuuint64_t(a.num_tokens)};
+    const cuuint64_t strides[2] = {cuuint64_t(kHeadDim) * 2, cuuint64_t(d.num_q_heads) * kHeadDim * 2};
+    const cuuint32_t box[3] = {64, cuuint32_t(G), cuuint32_t(tile_tokens(d))};
+    if (!encode(&tq, a.q, 3, dims, strides, box)) return PKV_ERR_LAUNCH;
+  }
+  {
+    const cuuint64_t rows = cuuint64_t(d.num_blocks) * d.num_kv_heads * kPage;
+    const cuuint64_t dims[2] = {cuuint64_t(kHeadDim), rows};
+    const cuuint64_t strides[1] = {cuuint64_t(kHeadDim) * 2};
+    const cuuint32_t box[2] = {64, cuuint32_t(kPage)};
+    if (!encode(&tk, a.k_cache, 2, dims, strides, box)) return PKV_ERR_LAUNCH;
+    if (!encode(&tv, a.v_cache, 2, dims, strides, box)) return PKV_ERR_LAUNCH;
+  }
+  PrefillParams pp{};
+  pp.block_tables = a.block_tables;
+  pp.seq_lens = a.seq_lens;
+  pp.qsl = a.query_start_loc;
+  pp.out = a.out;
+  pp.status = ctx.status;
+  pp.B = a.num_seqs;
+  pp.T = a.num_tokens;
+  pp.Hkv = d.num_kv_heads;
+  pp.Hq = d.num_q_heads;
+  pp.G = G;
+  pp.TM = tile_tokens(d);
+  pp.max_blocks = d.max_blocks_per_seq;
+  pp.num_blocks = d.num_blocks;
+  pp.split_max_q = split_max_q;
+  pp.qscale = a.scale * 1.4426950408889634f;
+  TraceScope ts(ctx.stream, PKV_K_PREFILL);
+  pkv_prefill_kernel<<<dim3(d.num_kv_heads, max_tiles), kPfThreads, kPfSmemBytes, ctx.stream>>>(
+      tq, tk, tv, pp);
+  return ts.done();
 }
 
 }  // namespace pkv

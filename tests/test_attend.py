@@ -178,3 +178,40 @@ def test_repeated_calls_reuse_workspace(pkvlib):
                        b.scale, workspace=ws) for _ in range(3)]
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+def _kernel_launches(batch, max_query_len):
+    meta = to_device(batch)
+    kc, vc = batch.k_cache.clone(), batch.v_cache.clone()
+    pkv.write(batch.k_new, batch.v_new, meta["slot_mapping"], kc, vc)
+    tr = pkv.Trace(64)
+    with tr:
+        out = pkv.attend(batch.q, kc, vc, meta["block_tables"], meta["seq_lens"],
+                         meta["query_start_loc"], batch.scale, max_query_len=max_query_len)
+    torch.cuda.synchronize()
+    counts = {k: tr.read(k)[1] for k in ("decode", "prefill")}
+    tr.close()
+    return counts, out, kc, vc
+
+
+def test_long_chunks_run_on_the_tensor_core_kernel(pkvlib):
+    b = make_batch([700, 300, 90], [200, 1, 90], 8, 2, seed=30, device="cuda")
+    counts, out, _, _ = _kernel_launches(b, 0)
+    assert counts == {"decode": 1, "prefill": 1}
+    k_ref, v_ref = oracle_write(b)
+    compare(out, oracle_attend(b, k_ref, v_ref), what="prefill full rows")
+    # a bound at or below the split threshold routes every row through split-KV
+    counts, out2, _, _ = _kernel_launches(b, 1)
+    assert counts == {"decode": 1, "prefill": 0}
+    compare(out2, oracle_attend(b, k_ref, v_ref), what="split-KV all rows")
+
+
+@pytest.mark.parametrize("hq,hkv,L,n", [(32, 8, 1100, 130), (16, 2, 257, 257), (8, 8, 640, 300),
+                                        (32, 2, 129, 33), (64, 4, 3000, 17)])
+def test_prefill_chunks_all_rows(pkvlib, hq, hkv, L, n):
+    """Chunks spanning several 128-key tiles with ragged ends, every row."""
+    b = make_batch([L, 40], [n, 1], hq, hkv, seed=L + n, device="cuda")
+    counts, out, _, _ = _kernel_launches(b, n)
+    assert counts["prefill"] == 1
+    k_ref, v_ref = oracle_write(b)
+    compare(out, oracle_attend(b, k_ref, v_ref), what=f"prefill {hq}/{hkv} L={L} n={n}")
