@@ -37,7 +37,7 @@ METRIC = "decode tokens/s and achieved HBM GB/s (fraction of 8 TB/s) per attend 
 NOMINAL_HBM_GBS = 8000.0
 KERNEL_SOURCES = ["paged_kv_cache_pkv_gb300/csrc/pkv_decode.cu",
                   "paged_kv_cache_pkv_gb300/csrc/pkv_common.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_cfg2.md")
 
 
 def parse():
@@ -62,6 +62,19 @@ def dist_init(args):
             torch.cuda.set_device(local)
         torch.distributed.init_process_group(backend)
     return rank, world, local
+
+
+def job_throughput(units_local, seconds_local, world, device=None):
+    """Whole-job throughput of independent replicas: the units every rank
+    processed divided by the slowest rank's time (max over ranks).
+    Returns (units per second, slowest seconds, total units)."""
+    if world > 1:
+        t = torch.tensor([seconds_local], dtype=torch.float64, device=device)
+        u = torch.tensor([units_local], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(u, op=torch.distributed.ReduceOp.SUM)
+        seconds_local, units_local = float(t.item()), float(u.item())
+    return units_local / seconds_local, seconds_local, units_local
 
 
 def kernel_hash():
@@ -256,11 +269,7 @@ def main():
         torch.distributed.barrier()
     clk = clocks.stop()
     step_ms = [a.elapsed_time(c) for a, c in ev]
-    total_s = sum(step_ms) / 1e3
-    if world > 1:
-        x = torch.tensor([total_s], device=dev)
-        torch.distributed.all_reduce(x, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(x.item())
+    value, total_s, _ = job_throughput(b.T * args.steps, sum(step_ms) / 1e3, world, dev)
     if pkv.get_last_error():
         raise RuntimeError("device status flags set during the timed region")
 
@@ -275,8 +284,6 @@ def main():
             step()
     torch.cuda.synchronize()
 
-    tokens = b.T * args.steps * world
-    value = tokens / total_s
     uniq = kv_bytes(b, unique=True)
     qo_bytes = 2 * b.q.numel() * 2
     meta_bytes = 4 * (b.block_tables.size + 2 * b.B + 1)
@@ -285,13 +292,15 @@ def main():
     dec_avg_s = dec_ms / max(dec_n, 1) / 1e3
     peaks, peak_kind = measured_peaks()
     achieved = alg_bytes / dec_avg_s / 1e9
+    # DRAM bytes per launch from the committed ncu summary, only while the
+    # kernel source still matches the one that was profiled
     traffic = None
     try:
         with open(TRAFFIC_FILE) as f:
-            tr = json.load(f)
-        if tr.get("kernel_hash") == kernel_hash() and tr.get("workload") == args.workload:
-            traffic = tr.get("dram_bytes_per_launch")
-    except (OSError, ValueError):
+            tr = dict(l.split(": ", 1) for l in f.read().splitlines() if ": " in l and " " not in l.split(": ")[0])
+        if tr.get("kernel_hash") == kernel_hash() and int(tr.get("workload", -1)) == args.workload:
+            traffic = int(tr["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
         pass
     per_kernel = {}
     for k in ("write", "plan", "decode", "merge", "prefill"):
@@ -327,12 +336,8 @@ def main():
         e2e_step()
         e_ev[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_s = sum(a.elapsed_time(c) for a, c in e_ev) / 1e3
-    if world > 1:
-        x = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(x, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(x.item())
-    e2e_value = b.T * e2e_steps * world / e2e_s
+    e2e_value, _, _ = job_throughput(b.T * e2e_steps, sum(a.elapsed_time(c) for a, c in e_ev) / 1e3,
+                                     world, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
