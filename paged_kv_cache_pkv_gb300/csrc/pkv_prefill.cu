@@ -28,10 +28,14 @@
 //  * O += P V: 8 tcgen05.mma into TMEM columns 128..255; V is the N-major
 //    (dims contiguous) operand.  V rows past the sequence end are zeroed in
 //    shared memory first so stale pool contents cannot reach O.
-//  * Warp roles: warps 0-7 run the softmax; warp 8 (one lane) issues every TMA
-//    copy and tcgen05.mma, so block-table loads and copy issue never sit on
-//    the softmax's path.  Softmax -> MMA hand-off is an mbarrier ("P ready",
-//    256 arrivals); MMA -> softmax is tcgen05.commit on "S ready" / "O done".
+//  * Warp roles: warps 0-7 run the softmax; warp 8 loads K tiles, warp 9
+//    loads V tiles (each refills a buffer as soon as the MMA that read it is
+//    done, with the next tile's block ids prefetched), warp 10 issues every
+//    tcgen05.mma.  Pipeline: S(i+2) is computed while the softmax of tile i
+//    runs, PV(i) under the softmax of tile i+1.  Hand-offs are mbarriers:
+//    TMA complete_tx for K/V, tcgen05.commit for S done / PV done, 256
+//    softmax arrivals for P ready (one barrier per double buffer, so no wait
+//    ever targets a phase more than one behind).
 //  * Every mbarrier wait is bounded; on expiry the CTA flags
 //    PKV_STATUS_TIMEOUT, lets its in-flight copies and MMAs land, frees TMEM
 //    and returns.
@@ -48,10 +52,10 @@
 namespace pkv {
 
 constexpr int kPfSoftmaxThreads = 256;  // two threads per query row (64 score columns each)
-constexpr int kPfThreads = kPfSoftmaxThreads + 32;  // + one warp issuing TMA and MMA
+constexpr int kPfThreads = kPfSoftmaxThreads + 96;  // + K-load, V-load and MMA warps
 constexpr int kPfKeys = 128;          // keys per K/V tile (8 pages)
 constexpr int kPfPagesPerTile = kPfKeys / kPage;
-constexpr uint32_t kTmemCols = 256;   // S: [0,128), O: [128,256)
+constexpr uint32_t kTmemCols = 512;   // S0: [0,128), S1: [128,256), O: [256,384)
 constexpr float kPfTau = 8.0f;
 
 // Shared-memory map (offsets from a 1024-byte aligned base).
@@ -59,9 +63,11 @@ constexpr uint32_t kHalfTile = 128 * 128;          // 128 rows x 64 bf16 = 16 Ki
 constexpr uint32_t kOffQ = 0;                      // [2 halves]
 constexpr uint32_t kOffK = kOffQ + 2 * kHalfTile;  // [2 bufs][2 halves]
 constexpr uint32_t kOffV = kOffK + 4 * kHalfTile;  // [2 bufs][2 halves]
-constexpr uint32_t kOffP = kOffV + 4 * kHalfTile;  // [2 halves]
-constexpr uint32_t kOffMisc = kOffP + 2 * kHalfTile;
-constexpr uint32_t kPfSmemBytes = kOffMisc + 2048 + 1024;  // + misc (barriers, row exchange) + alignment slack
+constexpr uint32_t kOffP = kOffV + 4 * kHalfTile;  // [2 bufs][2 halves]
+constexpr uint32_t kOffMisc = kOffP + 4 * kHalfTile;
+constexpr uint32_t kPfMisc = 1536;  // barriers, TMEM address, tile info, scan sums, row exchange
+constexpr uint32_t kPfSmemBytes = kOffMisc + kPfMisc + 1024;  // + alignment slack
+static_assert(kPfSmemBytes <= 232448, "prefill shared memory above the 227 KiB per-CTA limit");
 
 struct PrefillParams {
   const int32_t* block_tables;
@@ -198,16 +204,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint8_t* sK = sm + kOffK;
   uint8_t* sV = sm + kOffV;
   uint8_t* sP = sm + kOffP;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffMisc);  // q, kv0, kv1, s, o, p
-  uint64_t* bar_q = bars;
-  uint64_t* bar_kv = bars + 1;
-  uint64_t* bar_s = bars + 3;
-  uint64_t* bar_o = bars + 4;
-  uint64_t* bar_p = bars + 5;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 64);
-  int* s_info = reinterpret_cast<int*>(sm + kOffMisc + 72);  // b, t0, total tiles
+  // misc region: 16 barrier slots, TMEM address, tile info, row exchange
+  static_assert(11 * 8 <= 128 && 144 + 4 * (kPfThreads / 32) <= 256 && 256 + 2 * 128 * 4 <= kPfMisc,
+                "prefill misc region layout");
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffMisc);
+  uint64_t* bar_q = bars;       // Q landed
+  uint64_t* bar_k = bars + 1;   // [2] K tile landed in buffer b
+  uint64_t* bar_v = bars + 3;   // [2] V tile landed in buffer b
+  uint64_t* bar_s = bars + 5;   // [2] S of a tile computed into TMEM buffer b
+  uint64_t* bar_o = bars + 7;   // [2] PV that read P buffer b done
+  uint64_t* bar_p = bars + 9;   // [2] P buffer b written by the softmax (256 arrivals)
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 128);  // after 16 barrier slots
+  int* s_info = reinterpret_cast<int*>(sm + kOffMisc + 136);  // b, t0
   int* s_scan = reinterpret_cast<int*>(sP);  // plan scratch, reused by P later
-  __shared__ int s_wsum[kPfThreads / 32];
+  int* s_wsum = reinterpret_cast<int*>(sm + kOffMisc + 144);  // [warps] scan sums
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = blockIdx.x;  // kv head; blockIdx.y = tile (real tiles dispatch first)
@@ -278,8 +288,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   // ---- barriers and TMEM -----------------------------------------------------
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(bars + i, 1);
+    for (int i = 0; i < 9; ++i) mbar_init(bars + i, 1);
+    // One barrier per P buffer: the softmax can be a tile ahead of the MMA
+    // lane, never two on the same buffer (it needs PV(i) before P(i+2)).
     mbar_init(bar_p, kPfSoftmaxThreads);
+    mbar_init(bar_p + 1, kPfSoftmaxThreads);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -292,54 +305,76 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + 128;
+  const uint32_t tmem_o = tmem + 256;
   const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;  // warp w reads TMEM lanes 32*(w%4)..
+  auto tmem_s = [&](int buf) { return tmem + uint32_t(buf) * 128; };
+  const uint32_t idesc_s = idesc_bf16(128, 128, false);
+  const uint32_t idesc_o = idesc_bf16(128, 128, true);
+  const int role = warp - kPfSoftmaxThreads / 32;  // 0: K loads, 1: V loads, 2: MMA; < 0 softmax
 
-  // ---- producer helpers (thread 0) ---------------------------------------------
-  auto load_kv = [&](int kt, int buf) {
-    int valid = 0;
-    int bids[kPfPagesPerTile];
+  // block ids of the 8 pages of K/V tile kt (pages past the sequence: -1)
+  auto page_ids = [&](int kt, int (&bids)[kPfPagesPerTile]) {
 #pragma unroll
     for (int j = 0; j < kPfPagesPerTile; ++j) {
       const int pi = kt * kPfPagesPerTile + j;
-      int bid = -1;
-      if (pi < npages) {
-        bid = __ldg(p.block_tables + int64_t(b) * p.max_blocks + pi);
-        if (bid < 0 || bid >= p.num_blocks) {
-          flag_status(p.status, PKV_STATUS_BAD_BLOCK);
-          bid = 0;
-        }
-        ++valid;
-      }
-      bids[j] = bid;
+      bids[j] = pi < npages ? __ldg(p.block_tables + int64_t(b) * p.max_blocks + pi) : -1;
     }
-    mbar_arrive_expect_tx(bar_kv + buf, uint32_t(valid) * 4 * 2048);
+  };
+  auto load_tile = [&](const CUtensorMap* map, uint8_t* base, uint64_t* bar, const int (&bids)[kPfPagesPerTile]) {
+    int valid = 0;
+#pragma unroll
+    for (int j = 0; j < kPfPagesPerTile; ++j) valid += bids[j] >= 0;
+    mbar_arrive_expect_tx(bar, uint32_t(valid) * 2 * 2048);
 #pragma unroll
     for (int j = 0; j < kPfPagesPerTile; ++j) {
       if (bids[j] < 0) continue;
-      const int row = (bids[j] * p.Hkv + g) * kPage;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        tma_load_2d(sK + (buf * 2 + h) * kHalfTile + j * 2048, &tm_k, h * 64, row, bar_kv + buf);
-        tma_load_2d(sV + (buf * 2 + h) * kHalfTile + j * 2048, &tm_v, h * 64, row, bar_kv + buf);
+      int bid = bids[j];
+      if (bid >= p.num_blocks) {
+        flag_status(p.status, PKV_STATUS_BAD_BLOCK);
+        bid = 0;
       }
+      const int row = (bid * p.Hkv + g) * kPage;
+      tma_load_2d(base + j * 2048, map, 0, row, bar);
+      tma_load_2d(base + kHalfTile + j * 2048, map, 64, row, bar);
     }
   };
 
-  const uint32_t idesc_s = idesc_bf16(128, 128, false);
-  const uint32_t idesc_o = idesc_bf16(128, 128, true);
-  const bool mma_warp = warp == kPfSoftmaxThreads / 32;
-
-  if (mma_warp) {
-    // ===== TMA + MMA issuer (one lane) =====
+  if (role == 0 || role == 1) {
+    // ===== K or V producer (one lane) =====
+    // Buffer kt&1 is free once the MMA that read tile kt-2 is done: S for K,
+    // PV for V.  Block ids of the next tile are in flight while waiting.
     if (lane == 0) {
-      int issued = 0, n_s = 0, n_pv = 0;
+      const CUtensorMap* map = role == 0 ? &tm_k : &tm_v;
+      uint8_t* base0 = role == 0 ? sK : sV;
+      uint64_t* bar_load = role == 0 ? bar_k : bar_v;
+      uint64_t* bar_free = role == 0 ? bar_s : bar_o;
+      if (role == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+        mbar_arrive_expect_tx(bar_q, 2 * kHalfTile);
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sQ + h * kHalfTile, &tm_q, h * 64, g * p.G, q0 + t0, bar_q);
+      }
+      int ids[kPfPagesPerTile], next[kPfPagesPerTile];
+      page_ids(0, ids);
+      int loaded = 0;
       bool ok = true;
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
-      mbar_arrive_expect_tx(bar_q, 2 * kHalfTile);
-      for (int h = 0; h < 2; ++h)
-        tma_load_3d(sQ + h * kHalfTile, &tm_q, h * 64, g * p.G, q0 + t0, bar_q);
-      for (; issued < min(2, nkv); ++issued) load_kv(issued, issued & 1);
+      for (int kt = 0; kt < nkv; ++kt) {
+        if (kt + 1 < nkv) page_ids(kt + 1, next);
+        if (kt >= 2 && !(ok = mbar_wait(bar_free + (kt & 1), ((kt - 2) >> 1) & 1))) break;
+        load_tile(map, base0 + (kt & 1) * 2 * kHalfTile, bar_load + (kt & 1), ids);
+        ++loaded;
+#pragma unroll
+        for (int j = 0; j < kPfPagesPerTile; ++j) ids[j] = next[j];
+      }
+      // copies land before the CTA's shared memory is released
+      for (int k = max(0, loaded - 2); k < loaded; ++k)
+        mbar_wait(bar_load + (k & 1), (k >> 1) & 1, ok ? kWaitLimitNs : kDrainLimitNs);
+      if (!ok) flag_status(p.status, PKV_STATUS_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (role == 2) {
+    // ===== MMA issuer (one lane) =====
+    if (lane == 0) {
       auto issue_s = [&](int kt) {
         const int buf = kt & 1;
         tc_fence_after();
@@ -348,46 +383,40 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const int h = ks >> 2, kk = ks & 3;
           const uint64_t a = smem_desc(smem_u32(sQ + h * kHalfTile) + kk * 32, 16, 1024);
           const uint64_t bdesc = smem_desc(smem_u32(sK + (buf * 2 + h) * kHalfTile) + kk * 32, 16, 1024);
-          umma(tmem_s, a, bdesc, idesc_s, ks > 0);
+          umma(tmem_s(buf), a, bdesc, idesc_s, ks > 0);
         }
-        umma_commit(bar_s);
-        ++n_s;
+        umma_commit(bar_s + buf);
       };
-      ok = mbar_wait(bar_q, 0) && mbar_wait(bar_kv, 0);
-      if (ok) issue_s(0);
+      int ns = 0, npv = 0;
+      bool ok = mbar_wait(bar_q, 0);
+      for (; ok && ns < min(2, nkv); ++ns) {
+        if (!(ok = mbar_wait(bar_k + ns, 0))) break;
+        issue_s(ns);
+      }
       for (int it = 0; ok && it < nkv; ++it) {
-        const int buf = it & 1;
-        // P of tile it is in shared memory (and O rescaled if needed)
-        if (!(ok = mbar_wait(bar_p, it & 1))) break;
+        const int buf = it & 1, ph = (it >> 1) & 1;
+        // P(it) written by the softmax (which also released S buffer buf); V(it) landed
+        if (!(ok = mbar_wait(bar_p + buf, ph) && mbar_wait(bar_v + buf, ph))) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const int h = ks >> 2, kk = ks & 3;
-          const uint64_t a = smem_desc(smem_u32(sP + h * kHalfTile) + kk * 32, 16, 1024);
+          const uint64_t a = smem_desc(smem_u32(sP + (buf * 2 + h) * kHalfTile) + kk * 32, 16, 1024);
           const uint64_t bdesc = smem_desc(smem_u32(sV + buf * 2 * kHalfTile) + ks * 2048, kHalfTile, 1024);
           umma(tmem_o, a, bdesc, idesc_o, (it > 0 || ks > 0) ? 1u : 0u);
         }
-        umma_commit(bar_o);
-        ++n_pv;
-        if (it + 1 < nkv) {
-          if (!(ok = mbar_wait(bar_kv + ((it + 1) & 1), ((it + 1) >> 1) & 1))) break;
-          issue_s(it + 1);
-        }
-        if (issued < nkv) {  // tile it's buffer frees once PV(it) is done
-          if (!(ok = mbar_wait(bar_o, it & 1))) break;
-          load_kv(issued, issued & 1);
-          ++issued;
+        umma_commit(bar_o + buf);
+        ++npv;
+        if (ns < nkv) {  // ns == it + 2
+          if (!(ok = mbar_wait(bar_k + buf, (ns >> 1) & 1))) break;
+          issue_s(ns++);
         }
       }
       if (!ok) {
         flag_status(p.status, PKV_STATUS_TIMEOUT);
-        // Let what was issued land before TMEM and shared memory are released:
-        // the newest copy on each buffer and the newest commit of each kind
-        // (older phases completed before these were issued).
-        for (int k = max(0, issued - 2); k < issued; ++k)
-          mbar_wait(bar_kv + (k & 1), (k >> 1) & 1, kDrainLimitNs);
-        if (n_s > 0) mbar_wait(bar_s, (n_s - 1) & 1, kDrainLimitNs);
-        if (n_pv > 0) mbar_wait(bar_o, (n_pv - 1) & 1, kDrainLimitNs);
+        // the newest commit of each kind lands before TMEM is released
+        for (int k = max(0, ns - 2); k < ns; ++k) mbar_wait(bar_s + (k & 1), (k >> 1) & 1, kDrainLimitNs);
+        for (int k = max(0, npv - 2); k < npv; ++k) mbar_wait(bar_o + (k & 1), (k >> 1) & 1, kDrainLimitNs);
       }
     }
     __syncwarp();
@@ -399,19 +428,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const bool row_valid = t0 + t_rel < n;
     const int pos = row_valid ? L - n + t0 + t_rel : L - 1;
     float m = -INFINITY, l = 0.f;  // running max (same in both threads of a row), half row sum
-    float* s_red = reinterpret_cast<float*>(sm + kOffMisc + 128);  // [2][128] exchange
+    float* s_red = reinterpret_cast<float*>(sm + kOffMisc + 256);  // [2][128] exchange
     bool ok = true;
     for (int it = 0; it < nkv; ++it) {
-      const int buf = it & 1;
-      ok = mbar_wait(bar_s, it & 1);
-      if (it > 0) ok = ok && mbar_wait(bar_o, (it - 1) & 1);
+      const int buf = it & 1, ph = (it >> 1) & 1;
+      ok = mbar_wait(bar_s + buf, ph);
+      // P buffer `buf` was last read by PV(it-2)
+      if (it >= 2) ok = ok && mbar_wait(bar_o + buf, ph ^ 1);
       tc_fence_after();
       // ---- this thread's 64 columns of row r ----
       const int kbase = it * kPfKeys + ch * 64;
       // no masking in this half tile for any row of the warp: the pass below
       // runs warp-collective TMEM loads, so the choice must be warp-uniform
       const bool full = __all_sync(0xffffffffu, kbase + 63 <= pos);
-      const uint32_t scol = tmem_s + lane_off + ch * 64;
+      const uint32_t scol = tmem_s(buf) + lane_off + ch * 64;
       uint32_t pk[2][16];
       float mx = -INFINITY, rs = 0.f;
       // One pass over the 64 columns: exp2(s*scale - mref) packed to bf16,
@@ -464,14 +494,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         alpha = m == -INFINITY ? 0.f : ex2(m - row_mx);
         m = row_mx;
       }
+      const bool warp_grow = __any_sync(0xffffffffu, grow);
       // redo the pass against the new maximum; warp-uniform (TMEM loads are
       // warp-collective), rows whose maximum did not move recompute the same P
-      if (__any_sync(0xffffffffu, grow)) {
+      if (warp_grow) {
         if (full) pass(m, std::true_type{}, std::false_type{});
         else pass(m, std::false_type{}, std::false_type{});
       }
       l = l * alpha + rs;
-      uint8_t* prow = sP + r * 128;
+      uint8_t* prow = sP + buf * 2 * kHalfTile + r * 128;
 #pragma unroll
       for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -480,8 +511,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           uint4* dst = reinterpret_cast<uint4*>(prow + ch * kHalfTile + ((chunk ^ (r & 7)) << 4));
           *dst = make_uint4(pk[c][4 * q], pk[c][4 * q + 1], pk[c][4 * q + 2], pk[c][4 * q + 3]);
         }
-      // rescale this thread's 64 O columns when the running max moved
-      if (it > 0 && __any_sync(0xffffffffu, grow)) {
+      // rescale this thread's 64 O columns when the running max moved; O is
+      // final up to PV(it-1), which must have finished
+      if (it > 0 && warp_grow) {
+        const bool done = mbar_wait(bar_o + (buf ^ 1), ((it - 1) >> 1) & 1);
+        ok = ok && done;
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t ov[32];
@@ -493,18 +528,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         tmem_wait_st();
       }
-      // keys past the sequence end: zero their V rows so stale data cannot leak
-      if (it * kPfKeys + r >= L) {
-        uint4* vrow = reinterpret_cast<uint4*>(sV + (buf * 2 + ch) * kHalfTile + r * 128);
+      // keys past the sequence end: zero their V rows (after V landed) so
+      // stale pool contents cannot leak through P = 0
+      if ((it + 1) * kPfKeys > L) {
+        ok = mbar_wait(bar_v + buf, ph) && ok;
+        if (it * kPfKeys + r >= L) {
+          uint4* vrow = reinterpret_cast<uint4*>(sV + (buf * 2 + ch) * kHalfTile + r * 128);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) vrow[q] = make_uint4(0, 0, 0, 0);
+          for (int q = 0; q < 8; ++q) vrow[q] = make_uint4(0, 0, 0, 0);
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar_p);  // P of this tile is ready for the MMA warp
+      mbar_arrive(bar_p + buf);  // P of this tile is ready for the MMA warp
     }
     // ---- epilogue: O / l -> bf16, each thread its 64 columns of row r ----
-    ok = ok && mbar_wait(bar_o, (nkv - 1) & 1);
+    ok = ok && mbar_wait(bar_o + ((nkv - 1) & 1), ((nkv - 1) >> 1) & 1);
     s_red[ch * 128 + r] = l;
     named_sync(1, kPfSoftmaxThreads);
     tc_fence_after();
