@@ -17,16 +17,18 @@
 //    page ids come from the block table, pages past the sequence are skipped.
 //    K/V tiles are double-buffered: tile i+1 loads while tile i computes.
 //  * S = Q K^T: 8 tcgen05.mma (M=128, N=128, K=16, bf16 in, fp32 out) into
-//    TMEM columns 0..127; both operands K-major in shared memory.
+//    one of two TMEM buffers (columns 0..127 / 128..255); both operands
+//    K-major in shared memory.
 //  * Softmax: threads t and t+128 own TMEM lane t%128 (query row t%128), 64
 //    score columns each: tcgen05.ld, bottom-right causal mask, exp2 against
 //    the running max in the log2 domain, row max exchanged through shared
 //    memory.  The running max only moves when a score exceeds it by more than
 //    kTau (then the pass is redone and O in TMEM is rescaled), so most tiles
-//    take one pass.  P is rounded to bf16 into shared memory in the same
-//    swizzled K-major layout.
-//  * O += P V: 8 tcgen05.mma into TMEM columns 128..255; V is the N-major
-//    (dims contiguous) operand.  V rows past the sequence end are zeroed in
+//    take one pass.  P is rounded to bf16 and stored into TMEM (two bf16 per
+//    32-bit column, row = lane), where the PV MMA reads its A operand: no
+//    shared-memory traffic for P.
+//  * O += P V: 8 tcgen05.mma (A from TMEM) into TMEM columns 256..383; V is
+//    the N-major (dims contiguous) operand in shared memory.  V rows past the sequence end are zeroed in
 //    shared memory first so stale pool contents cannot reach O.
 //  * Warp roles: warps 0-7 run the softmax; warp 8 loads K tiles, warp 9
 //    loads V tiles (each refills a buffer as soon as the MMA that read it is
@@ -55,16 +57,15 @@ constexpr int kPfSoftmaxThreads = 256;  // two threads per query row (64 score c
 constexpr int kPfThreads = kPfSoftmaxThreads + 96;  // + K-load, V-load and MMA warps
 constexpr int kPfKeys = 128;          // keys per K/V tile (8 pages)
 constexpr int kPfPagesPerTile = kPfKeys / kPage;
-constexpr uint32_t kTmemCols = 512;   // S0: [0,128), S1: [128,256), O: [256,384)
+constexpr uint32_t kTmemCols = 512;   // S0 [0,128), S1 [128,256), O [256,384), P0 [384,448), P1 [448,512)
 constexpr float kPfTau = 8.0f;
 
-// Shared-memory map (offsets from a 1024-byte aligned base).
+// Shared-memory map (offsets from a 1024-byte aligned base); P lives in TMEM.
 constexpr uint32_t kHalfTile = 128 * 128;          // 128 rows x 64 bf16 = 16 KiB
 constexpr uint32_t kOffQ = 0;                      // [2 halves]
 constexpr uint32_t kOffK = kOffQ + 2 * kHalfTile;  // [2 bufs][2 halves]
 constexpr uint32_t kOffV = kOffK + 4 * kHalfTile;  // [2 bufs][2 halves]
-constexpr uint32_t kOffP = kOffV + 4 * kHalfTile;  // [2 bufs][2 halves]
-constexpr uint32_t kOffMisc = kOffP + 4 * kHalfTile;
+constexpr uint32_t kOffMisc = kOffV + 4 * kHalfTile;
 constexpr uint32_t kPfMisc = 1536;  // barriers, TMEM address, tile info, scan sums, row exchange
 constexpr uint32_t kPfSmemBytes = kOffMisc + kPfMisc + 1024;  // + alignment slack
 static_assert(kPfSmemBytes <= 232448, "prefill shared memory above the 227 KiB per-CTA limit");
@@ -106,6 +107,16 @@ __device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, ui
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// Same, with the A operand (M rows x K, two bf16 per 32-bit column) in TMEM.
+__device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -203,7 +214,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint8_t* sQ = sm + kOffQ;
   uint8_t* sK = sm + kOffK;
   uint8_t* sV = sm + kOffV;
-  uint8_t* sP = sm + kOffP;
   // misc region: 16 barrier slots, TMEM address, tile info, row exchange
   static_assert(11 * 8 <= 128 && 144 + 4 * (kPfThreads / 32) <= 256 && 256 + 2 * 128 * 4 <= kPfMisc,
                 "prefill misc region layout");
@@ -216,7 +226,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t* bar_p = bars + 9;   // [2] P buffer b written by the softmax (256 arrivals)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 128);  // after 16 barrier slots
   int* s_info = reinterpret_cast<int*>(sm + kOffMisc + 136);  // b, t0
-  int* s_scan = reinterpret_cast<int*>(sP);  // plan scratch, reused by P later
+  int* s_scan = reinterpret_cast<int*>(sK);  // plan scratch (before any K tile lands)
   int* s_wsum = reinterpret_cast<int*>(sm + kOffMisc + 144);  // [warps] scan sums
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -308,6 +318,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t tmem_o = tmem + 256;
   const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;  // warp w reads TMEM lanes 32*(w%4)..
   auto tmem_s = [&](int buf) { return tmem + uint32_t(buf) * 128; };
+  auto tmem_p = [&](int buf) { return tmem + 384 + uint32_t(buf) * 64; };
   const uint32_t idesc_s = idesc_bf16(128, 128, false);
   const uint32_t idesc_o = idesc_bf16(128, 128, true);
   const int role = warp - kPfSoftmaxThreads / 32;  // 0: K loads, 1: V loads, 2: MMA; < 0 softmax
@@ -399,11 +410,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (!(ok = mbar_wait(bar_p + buf, ph) && mbar_wait(bar_v + buf, ph))) break;
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const int h = ks >> 2, kk = ks & 3;
-          const uint64_t a = smem_desc(smem_u32(sP + (buf * 2 + h) * kHalfTile) + kk * 32, 16, 1024);
+        for (int ks = 0; ks < 8; ++ks) {  // 16 keys = 8 packed TMEM columns of P
           const uint64_t bdesc = smem_desc(smem_u32(sV + buf * 2 * kHalfTile) + ks * 2048, kHalfTile, 1024);
-          umma(tmem_o, a, bdesc, idesc_o, (it > 0 || ks > 0) ? 1u : 0u);
+          umma_ts(tmem_o, tmem_p(buf) + ks * 8, bdesc, idesc_o, (it > 0 || ks > 0) ? 1u : 0u);
         }
         umma_commit(bar_o + buf);
         ++npv;
@@ -433,7 +442,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     for (int it = 0; it < nkv; ++it) {
       const int buf = it & 1, ph = (it >> 1) & 1;
       ok = mbar_wait(bar_s + buf, ph);
-      // P buffer `buf` was last read by PV(it-2)
+      // TMEM P buffer `buf` was last read by PV(it-2)
       if (it >= 2) ok = ok && mbar_wait(bar_o + buf, ph ^ 1);
       tc_fence_after();
       // ---- this thread's 64 columns of row r ----
@@ -502,15 +511,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         else pass(m, std::false_type{}, std::false_type{});
       }
       l = l * alpha + rs;
-      uint8_t* prow = sP + buf * 2 * kHalfTile + r * 128;
+      // P (bf16 pairs) into TMEM: row r, keys ch*64 .. ch*64+63 = 32 columns
+      {
+        uint32_t pw[32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int chunk = c * 4 + q;  // 16-byte chunk of the 128-byte row in half ch
-          uint4* dst = reinterpret_cast<uint4*>(prow + ch * kHalfTile + ((chunk ^ (r & 7)) << 4));
-          *dst = make_uint4(pk[c][4 * q], pk[c][4 * q + 1], pk[c][4 * q + 2], pk[c][4 * q + 3]);
+        for (int e = 0; e < 16; ++e) {
+          pw[e] = pk[0][e];
+          pw[16 + e] = pk[1][e];
         }
+        tmem_st32(tmem_p(buf) + lane_off + ch * 32, pw);
+        tmem_wait_st();
+      }
       // rescale this thread's 64 O columns when the running max moved; O is
       // final up to PV(it-1), which must have finished
       if (it > 0 && warp_grow) {
