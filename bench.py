@@ -234,15 +234,18 @@ def main():
     kc, vc = b.k_cache, b.v_cache
     out = torch.empty_like(b.q)
     desc = pkv.make_desc(kc, b.num_q_heads, bt.shape[1])
-    ws = torch.empty(pkv.workspace_size(desc, b.B, b.T, dev), dtype=torch.uint8, device=dev)
+    ws = torch.empty(pkv.workspace_size(desc, b.B, b.T, dev, int(b.info.get("shared_prefix_pages", 0))),
+                     dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     max_q = int(b.q_lens.max())  # the scheduler knows its largest query chunk
+    prefix = int(b.info.get("shared_prefix_pages", 0))  # and the prefix its sequences share
 
     def step():
         pkv.write(b.k_new, b.v_new, slots, kc, vc)
-        pkv.attend(b.q, kc, vc, bt, lens, qsl, b.scale, out=out, workspace=ws, max_query_len=max_q)
+        pkv.attend(b.q, kc, vc, bt, lens, qsl, b.scale, out=out, workspace=ws, max_query_len=max_q,
+                   shared_prefix_pages=prefix)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -323,7 +326,7 @@ def main():
             dev_in[name].copy_(x, non_blocking=True)
         pkv.write(dev_in["k_new"], dev_in["v_new"], dev_in["slots"], kc, vc)
         pkv.attend(dev_in["q"], kc, vc, dev_in["bt"], dev_in["lens"], dev_in["qsl"], b.scale, out=out,
-                   workspace=ws, max_query_len=max_q)
+                   workspace=ws, max_query_len=max_q, shared_prefix_pages=prefix)
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(3):

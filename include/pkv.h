@@ -119,9 +119,11 @@ PKV_API int pkv_write(const pkv_bf16* k_new, const pkv_bf16* v_new,
 #define PKV_SPLITKV_MAX_QLEN 8
 
 /* Workspace bytes pkv_attend needs on the CURRENT device for a batch of up
- * to num_seqs sequences and num_tokens query rows.  Writes *bytes. */
+ * to num_seqs sequences and num_tokens query rows (and shared_prefix_pages as
+ * passed to pkv_attend).  Writes *bytes. */
 PKV_API int pkv_attend_workspace_size(const pkv_desc* desc, int32_t num_seqs,
-                              int32_t num_tokens, size_t* bytes);
+                              int32_t num_tokens, int32_t shared_prefix_pages,
+                              size_t* bytes);
 
 /* pkv_attend -- paged grouped-query attention of one continuous batch.
  *   q             [num_tokens, num_q_heads, head_dim] bf16, device.
@@ -144,6 +146,16 @@ PKV_API int pkv_attend_workspace_size(const pkv_desc* desc, int32_t num_seqs,
  *                 most that threshold the prefill kernel is not launched and
  *                 split-KV takes every row, so a wrong bound never changes
  *                 results.
+ *   shared_prefix_pages  0, or P > 0 when the first P entries of EVERY
+ *                 block_tables row name the same pages: a prefix all the
+ *                 sequences share (read-only; llm-d blog, prefix-cache
+ *                 paragraphs).  Every query row is then attended to those
+ *                 pages once, on the tensor cores, and split-KV reads only
+ *                 each sequence's own pages after them, merging both parts
+ *                 (cascade).  Rows of sequences on the split-KV path must have
+ *                 at least one visible key past the prefix (else their
+ *                 sequence is skipped and PKV_STATUS_BAD_QUERY is set); the
+ *                 prefix is read through row 0 of block_tables.
  *   scale         softmax scale applied to q.k (e.g. 1/sqrt(head_dim)).
  *   out           [num_tokens, num_q_heads, head_dim] bf16, device; rows at
  *                 or beyond query_start_loc[num_seqs] are not written.
@@ -154,8 +166,8 @@ PKV_API int pkv_attend(const pkv_bf16* q, const pkv_bf16* k_cache,
                const pkv_bf16* v_cache, const int32_t* block_tables,
                const int32_t* seq_lens, const int32_t* query_start_loc,
                int32_t num_seqs, int32_t num_tokens, int32_t max_query_len,
-               float scale, pkv_bf16* out, void* workspace,
-               size_t workspace_bytes, const pkv_desc* desc,
+               int32_t shared_prefix_pages, float scale, pkv_bf16* out,
+               void* workspace, size_t workspace_bytes, const pkv_desc* desc,
                pkv_stream_t stream);
 
 /* pkv_attend_static -- pkv_attend for callers that cannot allocate device
@@ -186,8 +198,9 @@ PKV_API int pkv_attend_static(const pkv_bf16* q, const pkv_bf16* k_cache,
                               const pkv_bf16* v_cache, const int32_t* block_tables,
                               const int32_t* seq_lens, const int32_t* query_start_loc,
                               int32_t num_seqs, int32_t num_tokens,
-                              int32_t max_query_len, float scale, pkv_bf16* out,
-                              const pkv_desc* desc, pkv_stream_t stream);
+                              int32_t max_query_len, int32_t shared_prefix_pages,
+                              float scale, pkv_bf16* out, const pkv_desc* desc,
+                              pkv_stream_t stream);
 
 /* Wait for `stream`, then read and clear the current device's status word
  * (PKV_STATUS_* bits) into *flags. */

@@ -50,11 +50,11 @@ class Desc(ctypes.Structure):
 _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
 _SIGS = {
     "pkv_write": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp, _vp, ctypes.POINTER(Desc), _vp]),
-    "pkv_attend_workspace_size": (ctypes.c_int, [ctypes.POINTER(Desc), _i32, _i32, ctypes.POINTER(_sz)]),
-    "pkv_attend": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_float, _vp,
-                                  _vp, _sz, ctypes.POINTER(Desc), _vp]),
-    "pkv_attend_static": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_float,
-                                         _vp, ctypes.POINTER(Desc), _vp]),
+    "pkv_attend_workspace_size": (ctypes.c_int, [ctypes.POINTER(Desc), _i32, _i32, _i32, ctypes.POINTER(_sz)]),
+    "pkv_attend": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, ctypes.c_float,
+                                  _vp, _vp, _sz, ctypes.POINTER(Desc), _vp]),
+    "pkv_attend_static": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                         ctypes.c_float, _vp, ctypes.POINTER(Desc), _vp]),
     "pkv_get_last_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
     "pkv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_launch_count": (ctypes.c_uint64, []),
@@ -135,22 +135,25 @@ def write(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None):
                "pkv_write")
 
 
-def workspace_size(desc, num_seqs, num_tokens, device=None):
+def workspace_size(desc, num_seqs, num_tokens, device=None, shared_prefix_pages=0):
     n = ctypes.c_size_t(0)
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
-        _check(lib().pkv_attend_workspace_size(ctypes.byref(desc), num_seqs, num_tokens, ctypes.byref(n)),
+        _check(lib().pkv_attend_workspace_size(ctypes.byref(desc), num_seqs, num_tokens,
+                                               int(shared_prefix_pages), ctypes.byref(n)),
                "pkv_attend_workspace_size")
     return n.value
 
 
 def attend(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, out=None,
-           workspace=None, stream=None, max_query_len=0):
+           workspace=None, stream=None, max_query_len=0, shared_prefix_pages=0):
     """Paged GQA attention of one continuous batch; returns ``out`` [T, Hq, D].
 
     ``workspace`` (uint8 CUDA tensor) may be passed to avoid an allocation by
     PyTorch's caching allocator on every call.  ``max_query_len`` is an
     optional host-side upper bound on query rows per sequence (0 = unknown);
-    it only selects kernels, never results."""
+    it only selects kernels, never results.  ``shared_prefix_pages`` > 0 says
+    the first that many block-table entries of every row are the same pages
+    (a common prefix), attended once for all rows (cascade)."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_cache, "k_cache", torch.bfloat16, 4)
     _need(v_cache, "v_cache", torch.bfloat16, 4)
@@ -170,7 +173,7 @@ def attend(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, 
         _need(out, "out", torch.bfloat16, 3)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
-    need = workspace_size(desc, B, T, q.device)
+    need = workspace_size(desc, B, T, q.device, shared_prefix_pages)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     else:
@@ -179,7 +182,8 @@ def attend(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, 
             raise ValueError(f"workspace needs {need} bytes, got {workspace.numel()}")
     with torch.cuda.device(q.device):
         _check(lib().pkv_attend(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens),
-                                _ptr(query_start_loc), B, T, int(max_query_len), float(scale), _ptr(out),
+                                _ptr(query_start_loc), B, T, int(max_query_len), int(shared_prefix_pages),
+                                float(scale), _ptr(out),
                                 _ptr(workspace), workspace.numel(), ctypes.byref(desc),
                                 _stream(q.device, stream)),
                "pkv_attend")

@@ -156,22 +156,23 @@ int pkv_write(const pkv_bf16* k_new, const pkv_bf16* v_new, const int64_t* slot_
 }
 
 int pkv_attend_workspace_size(const pkv_desc* desc, int32_t num_seqs, int32_t num_tokens,
-                              size_t* bytes) {
+                              int32_t shared_prefix_pages, size_t* bytes) {
   if (int e = check_desc(desc)) return e;
   if (!bytes) return PKV_ERR_NULL;
-  if (num_seqs < 0 || num_tokens < 0) return PKV_ERR_RANGE;
+  if (num_seqs < 0 || num_tokens < 0 || shared_prefix_pages < 0) return PKV_ERR_RANGE;
   int err = PKV_OK;
   const DeviceInfo* dev = current_device(&err);
   if (!dev) return err;
-  *bytes = attend_workspace_bytes(*dev, *desc, num_seqs, num_tokens);
+  *bytes = attend_workspace_bytes(*dev, *desc, num_seqs, num_tokens, shared_prefix_pages);
   return PKV_OK;
 }
 
 int pkv_attend(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
                const int32_t* block_tables, const int32_t* seq_lens,
                const int32_t* query_start_loc, int32_t num_seqs, int32_t num_tokens,
-               int32_t max_query_len, float scale, pkv_bf16* out, void* workspace,
-               size_t workspace_bytes, const pkv_desc* desc, pkv_stream_t stream) {
+               int32_t max_query_len, int32_t shared_prefix_pages, float scale, pkv_bf16* out,
+               void* workspace, size_t workspace_bytes, const pkv_desc* desc,
+               pkv_stream_t stream) {
   if (int e = check_desc(desc)) return e;
   if (num_seqs < 0 || num_tokens < 0) return PKV_ERR_RANGE;
   if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
@@ -184,9 +185,9 @@ int pkv_attend(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cac
     return PKV_ERR_ALIGN;
   LaunchCtx ctx;
   if (int e = make_ctx(stream, &ctx)) return e;
-  AttendArgs a{q,          k_cache,       v_cache, block_tables, seq_lens,
-               query_start_loc, num_seqs, num_tokens, max_query_len, scale,
-               out,        workspace,     workspace_bytes, *desc};
+  AttendArgs a{q,          k_cache,    v_cache,    block_tables,  seq_lens,
+               query_start_loc, num_seqs, num_tokens, max_query_len, shared_prefix_pages,
+               scale,      out,        workspace,  workspace_bytes, *desc};
   return launch_attend(ctx, a);
 }
 

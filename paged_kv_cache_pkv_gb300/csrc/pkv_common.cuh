@@ -40,13 +40,17 @@ __host__ __device__ constexpr int partial_floats(int heads) {
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // 200 ms
 constexpr uint64_t kDrainLimitNs = 2ull * 1000 * 1000;   // 2 ms for the clean-up path
 
+// Shared-prefix partial record: o[128] unnormalised, then m (log2 domain)
+// and l; padded to a 16-byte multiple.
+constexpr int kPrefixRec = 132;
+
 // Most sequences one pkv_attend call may carry (the per-sequence unit prefix
 // of the split-KV plan lives in shared memory).
 constexpr int kMaxSeqs = 2048;
 
 // Workspace carve-up; every piece starts 256-byte aligned.
 struct WorkspaceLayout {
-  size_t counters, partials, tiles, total;
+  size_t counters, partials, tiles, prefix, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -54,13 +58,15 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // counters_per_row: arrival counters per query row (items x warps per ring);
 // heads_per_warp sizes one partial slot; every decode warp owns two slots.
 inline WorkspaceLayout workspace_layout(int num_tokens, int counters_per_row, int nwarps,
-                                        int heads_per_warp, int max_tiles) {
+                                        int heads_per_warp, int max_tiles,
+                                        size_t prefix_records = 0) {
   WorkspaceLayout w{};
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t at = off; off = align_up(off + bytes, 256); return at; };
   w.counters = take(sizeof(unsigned long long) * size_t(num_tokens) * size_t(counters_per_row));
   w.partials = take(sizeof(float) * size_t(partial_floats(heads_per_warp)) * 2 * size_t(nwarps));
   w.tiles = take(sizeof(int32_t) * 4 * size_t(max_tiles));
+  w.prefix = take(sizeof(float) * size_t(kPrefixRec) * prefix_records);
   w.total = off;
   return w;
 }

@@ -62,6 +62,10 @@ struct DecodeParams {
   int32_t B, T, num_blocks, Hkv, Hq, G, nsub, max_blocks, simt_max_q, nwarps;
   float qscale;  // scale * log2(e)
   unsigned long long epoch;  // 48-bit call tag, never 0
+  // shared prefix: the first np pages of every row were attended by the
+  // prefix pass, whose partial records (chunks per row and head) are merged
+  int32_t np, chunks;
+  const float* prefix_part;  // [T][Hq][chunks][kPrefixRec]
 };
 
 struct StageDesc {
@@ -78,6 +82,7 @@ struct __align__(128) DecRing {
 
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr float kTau = 8.0f;  // log2-domain slack before the running max moves
+constexpr int kMinChunk = 4;  // fewest pages a decode warp is given
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -112,13 +117,14 @@ __device__ __forceinline__ void cursor_seq(Cursor& c, const SeqSmem& sq, int b) 
   c.L = sq.len[b];
 }
 
-__device__ __forceinline__ void cursor_row(Cursor& c) {
+// Visible keys of the row and its own (suffix) pages after the shared prefix.
+__device__ __forceinline__ void cursor_row(Cursor& c, int np) {
   c.nvis = c.L - c.n + c.j + 1;
-  c.npages = (c.nvis + kPage - 1) / kPage;
+  c.npages = (c.nvis + kPage - 1) / kPage - np;
 }
 
 __device__ __forceinline__ void cursor_bid(Cursor& c, const DecodeParams& p) {
-  int bid = __ldg(p.block_tables + int64_t(c.b) * p.max_blocks + c.page);
+  int bid = __ldg(p.block_tables + int64_t(c.b) * p.max_blocks + p.np + c.page);
   if (bid < 0 || bid >= p.num_blocks) {
     flag_status(p.status, PKV_STATUS_BAD_BLOCK);
     bid = 0;
@@ -139,44 +145,132 @@ __device__ __forceinline__ void cursor_advance(Cursor& c, const DecodeParams& p,
         while (sq.start[b + 1] == sq.start[b]) ++b;
         cursor_seq(c, sq, b);
       }
-      cursor_row(c);
+      cursor_row(c, p.np);
     }
   }
   cursor_bid(c, p);
 }
 
 // Log-sum-exp merge of the partials of one (row, head group) over warps
-// w0..w1; every lane owns 4 dims of each of the GH heads.
+// w0..w1.  Lane i reads partial w0+i's maxima and sums (32 partials per
+// round, reduced across the warp), then every lane accumulates 4 dims of each
+// of the GH heads over all partials with independent loads.
+// Record of the shared-prefix pass for (row, query head, chunk c).
+__device__ __forceinline__ const float* prefix_rec(const DecodeParams& p, int row, int head, int c) {
+  return p.prefix_part + ((size_t(row) * p.Hq + head) * p.chunks + c) * kPrefixRec;
+}
+
+// Shared-prefix records of (row, heads h0..h0+NH-1), read lane-parallel:
+// lane c < chunks holds chunk c's maximum and sum of every head.
+template <int NH>
+struct PrefixFold {
+  float pm[NH], pl[NH], w[NH];
+  __device__ __forceinline__ void load(const DecodeParams& p, int lane, int row, int h0) {
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      const bool mine = lane < p.chunks;
+      const float* rec = prefix_rec(p, row, h0 + h, mine ? lane : 0);
+      pm[h] = mine ? __ldcg(rec + 128) : -INFINITY;
+      pl[h] = mine ? __ldcg(rec + 129) : 0.f;
+    }
+  }
+  // raise M[h] to the records' maximum
+  __device__ __forceinline__ void max_into(float (&M)[NH]) const {
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      float x = pm[h];
+#pragma unroll
+      for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+      M[h] = fmaxf(M[h], x);
+    }
+  }
+  // per-lane weights against the final M; adds the records' sums into L
+  __device__ __forceinline__ void weigh(const float (&M)[NH], float (&L)[NH]) {
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      w[h] = pm[h] == -INFINITY ? 0.f : ex2(pm[h] - M[h]);
+      float x = w[h] * pl[h];
+#pragma unroll
+      for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      L[h] += x;
+    }
+  }
+};
+
 template <int GH>
 __device__ __forceinline__ void merge_item(const DecodeParams& p, int lane, int row, int h0,
                                            int item_start, int npages, int chunk) {
   const int w0 = item_start / chunk, w1 = (item_start + npages - 1) / chunk;
+  const int nparts = w1 - w0 + 1;
+  const int npre = p.np > 0 ? p.chunks : 0;  // shared-prefix records to fold in
+  auto base_of = [&](int w) {
+    return p.partials + size_t(2 * w + (item_start <= w * chunk ? 0 : 1)) * partial_floats(GH);
+  };
   float M[GH], L[GH];
 #pragma unroll
   for (int h = 0; h < GH; ++h) {
     M[h] = -INFINITY;
     L[h] = 0.f;
   }
-  auto slot_of = [&](int w) { return 2 * w + (item_start <= w * chunk ? 0 : 1); };
-  for (int w = w0; w <= w1; ++w) {
-    const float* base = p.partials + size_t(slot_of(w)) * partial_floats(GH);
+  for (int k0 = 0; k0 < nparts; k0 += 32) {
+    const int k = k0 + lane;
 #pragma unroll
-    for (int h = 0; h < GH; ++h) M[h] = fmaxf(M[h], __ldcg(base + h));
+    for (int h = 0; h < GH; ++h) {
+      float mk = k < nparts ? __ldcg(base_of(w0 + k) + h) : -INFINITY;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) mk = fmaxf(mk, __shfl_xor_sync(kFull, mk, o));
+      M[h] = fmaxf(M[h], mk);
+    }
+  }
+  PrefixFold<GH> pf;
+  if (npre) {
+    pf.load(p, lane, row, h0);
+    pf.max_into(M);
   }
   float4 acc[GH];
 #pragma unroll
   for (int h = 0; h < GH; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int w = w0; w <= w1; ++w) {
-    const float* base = p.partials + size_t(slot_of(w)) * partial_floats(GH);
+  for (int k0 = 0; k0 < nparts; k0 += 32) {
+    const int k = k0 + lane;
+    float sc_mine[GH];
 #pragma unroll
     for (int h = 0; h < GH; ++h) {
-      const float sc = ex2(__ldcg(base + h) - M[h]);
-      L[h] += sc * __ldcg(base + 4 + h);
-      const float4 x = __ldcg(reinterpret_cast<const float4*>(base + kPartialHeader + h * kHeadDim) + lane);
-      acc[h].x += sc * x.x;
-      acc[h].y += sc * x.y;
-      acc[h].z += sc * x.z;
-      acc[h].w += sc * x.w;
+      const float* b = base_of(w0 + min(k, nparts - 1));
+      const float sc = k < nparts ? ex2(__ldcg(b + h) - M[h]) : 0.f;
+      float lk = sc * (k < nparts ? __ldcg(b + 4 + h) : 0.f);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) lk += __shfl_xor_sync(kFull, lk, o);
+      L[h] += lk;
+      sc_mine[h] = sc;
+    }
+    const int cnt = min(32, nparts - k0);
+#pragma unroll 4
+    for (int i = 0; i < cnt; ++i) {
+      const float* b = base_of(w0 + k0 + i);
+#pragma unroll
+      for (int h = 0; h < GH; ++h) {
+        const float sc = __shfl_sync(kFull, sc_mine[h], i);
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(b + kPartialHeader + h * kHeadDim) + lane);
+        acc[h].x += sc * x.x;
+        acc[h].y += sc * x.y;
+        acc[h].z += sc * x.z;
+        acc[h].w += sc * x.w;
+      }
+    }
+  }
+  if (npre) {
+    pf.weigh(M, L);
+#pragma unroll 4
+    for (int c = 0; c < npre; ++c) {
+#pragma unroll
+      for (int h = 0; h < GH; ++h) {
+        const float sc = __shfl_sync(kFull, pf.w[h], c);
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(prefix_rec(p, row, h0 + h, c)) + lane);
+        acc[h].x += sc * x.x;
+        acc[h].y += sc * x.y;
+        acc[h].z += sc * x.z;
+        acc[h].w += sc * x.w;
+      }
     }
   }
 #pragma unroll
@@ -226,8 +320,14 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
                        (L + kPage - 1) / kPage > p.max_blocks || (b == 0 && q0 != 0);
       if (bad && blockIdx.x == 0) flag_status(p.status, PKV_STATUS_BAD_QUERY);
       int units = 0;
-      if (!bad && n >= 1 && n <= p.simt_max_q)
-        units = int(pages_prefix(L) - pages_prefix(L - n)) * per_row;
+      if (!bad && n >= 1 && n <= p.simt_max_q) {
+        if (p.np > 0 && L - n + 1 <= p.np * kPage) {
+          // every split-KV row needs a key of its own past the shared prefix
+          if (blockIdx.x == 0) flag_status(p.status, PKV_STATUS_BAD_QUERY);
+        } else {
+          units = int(pages_prefix(L) - pages_prefix(L - n) - int64_t(n) * p.np) * per_row;
+        }
+      }
       s_start[b] = units;
       local += units;
     }
@@ -255,7 +355,9 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
     __syncthreads();
   }
   const int U = s_start[p.B];
-  const int chunk = max(1, (U + p.nwarps - 1) / p.nwarps);
+  // equal contiguous ranges, at least kMinChunk pages so small batches do not
+  // shatter into one-page partials
+  const int chunk = max(kMinChunk, (U + p.nwarps - 1) / p.nwarps);
   const int w = blockIdx.x * kDecWarps + wib;
   if (w >= p.nwarps || int64_t(w) * chunk >= U) return;
   const int u_begin = w * chunk;
@@ -273,11 +375,11 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
     cursor_seq(pc, sq, lo);
     int local = u_begin - s_start[lo];
     pc.j = 0;
-    cursor_row(pc);
+    cursor_row(pc, p.np);
     while (local >= pc.npages * per_row) {
       local -= pc.npages * per_row;
       ++pc.j;
-      cursor_row(pc);
+      cursor_row(pc, p.np);
     }
     pc.item = local / pc.npages;
     pc.page = local - pc.item * pc.npages;
@@ -288,7 +390,7 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
     if (lane == 0) {
       const int g = pc.item / p.nsub;
       const size_t off = (size_t(pc.bid) * p.Hkv + g) * (kPageBytes / 2);
-      R.desc[stage] = StageDesc{pc.q0 + pc.j, pc.item, pc.item_start, pc.nvis};
+      R.desc[stage] = StageDesc{pc.q0 + pc.j, pc.item, pc.item_start, pc.nvis - p.np * kPage};
       mbar_arrive_expect_tx(&R.bar[stage], 2 * kPageBytes);
       bulk_g2s(&R.kv[stage][0][0], p.k_cache + off, kPageBytes, &R.bar[stage], policy);
       bulk_g2s(&R.kv[stage][1][0], p.v_cache + off, kPageBytes, &R.bar[stage], policy);
@@ -386,22 +488,76 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
         if (x == h) v = o[x][e];
       return v;
     };
+    // shared-prefix fold for the whole-item write (all lanes take part)
+    PrefixFold<GH> pf;
+    float self_w[GH], Lf[GH];
+    // the writes below run on the writer lanes only (all 32, or lanes 0-15
+    // when GH == 1); chunk weights come from lanes < chunks <= 16
+    const unsigned pf_mask = GH >= 2 ? 0xffffffffu : 0x0000ffffu;
+    if (whole && p.np > 0) {
+      float M[GH];
+#pragma unroll
+      for (int x = 0; x < GH; ++x) M[x] = m[x];
+      pf.load(p, lane, cur_row, cur_h0);
+      pf.max_into(M);
+#pragma unroll
+      for (int x = 0; x < GH; ++x) {
+        self_w[x] = ex2(m[x] - M[x]);
+        Lf[x] = self_w[x] * l[x];
+      }
+      pf.weigh(M, Lf);
+    }
     if (whole) {
       if (writer) {
 #pragma unroll
         for (int hh = 0; hh < HPL; ++hh) {
           const int h = (GH >= 2 ? par * HPL : 0) + hh;
-          float lh = l[0];
+          float lh = l[0], mh = m[0];
 #pragma unroll
           for (int x = 0; x < GH; ++x)
-            if (x == h) lh = l[x];
+            if (x == h) {
+              lh = l[x];
+              mh = m[x];
+            }
+          float2 v[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] = pick(h, e);
+          if (p.np > 0) {  // fold in the shared-prefix records of this head
+            float ws = 1.f;
+#pragma unroll
+            for (int x = 0; x < GH; ++x)
+              if (x == h) {
+                ws = self_w[x];
+                lh = Lf[x];
+              }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = make_float2(v[e].x * ws, v[e].y * ws);
+#pragma unroll 4
+            for (int c = 0; c < p.chunks; ++c) {
+              // lane c holds chunk c's weights of every head; take head h's
+              float sc = 0.f;
+#pragma unroll
+              for (int x = 0; x < GH; ++x) {
+                const float sx = __shfl_sync(pf_mask, pf.w[x], c);
+                if (x == h) sc = sx;
+              }
+              const float* rec = prefix_rec(p, cur_row, cur_h0 + h, c);
+              const float4 a = __ldcg(reinterpret_cast<const float4*>(rec + dc * 8));
+              const float4 b2 = __ldcg(reinterpret_cast<const float4*>(rec + dc * 8 + 4));
+              v[0].x += sc * a.x;
+              v[0].y += sc * a.y;
+              v[1].x += sc * a.z;
+              v[1].y += sc * a.w;
+              v[2].x += sc * b2.x;
+              v[2].y += sc * b2.y;
+              v[3].x += sc * b2.z;
+              v[3].y += sc * b2.w;
+            }
+          }
           const float inv = 1.f / lh;
           uint32_t pk[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 v = pick(h, e);
-            pk[e] = pack_bf16x2(v.x * inv, v.y * inv);
-          }
+          for (int e = 0; e < 4; ++e) pk[e] = pack_bf16x2(v[e].x * inv, v[e].y * inv);
           *reinterpret_cast<uint4*>(p.out + (size_t(cur_row) * p.Hq + cur_h0 + h) * kHeadDim + dc * 8) =
               make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
@@ -708,12 +864,19 @@ static unsigned long long next_epoch() {
   }
 }
 
+static size_t prefix_records(const pkv_desc& d, int32_t num_tokens, int32_t prefix_pages) {
+  int ct = 0;
+  const int chunks = prefix_chunks(d, num_tokens, prefix_pages, &ct);
+  return size_t(num_tokens) * d.num_q_heads * size_t(chunks);
+}
+
 size_t attend_workspace_bytes(const DeviceInfo& dev, const pkv_desc& d, int32_t num_seqs,
-                              int32_t num_tokens) {
+                              int32_t num_tokens, int32_t shared_prefix_pages) {
   const int G = d.num_q_heads / d.num_kv_heads;
   const int gh = group_per_item(G);
   return workspace_layout(num_tokens, d.num_kv_heads * (G / gh), dev.dec_warps[variant_of(gh)], gh,
-                          prefill_max_tiles(d, num_seqs, num_tokens))
+                          prefill_max_tiles(d, num_seqs, num_tokens),
+                          prefix_records(d, num_tokens, shared_prefix_pages))
       .total;
 }
 
@@ -746,8 +909,12 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   if (int64_t(a.num_tokens) * d.max_blocks_per_seq * d.num_kv_heads * nsub >= (int64_t(1) << 31))
     return PKV_ERR_RANGE;
   const int max_tiles = prefill_max_tiles(d, a.num_seqs, a.num_tokens);
+  if (a.shared_prefix_pages < 0 || a.shared_prefix_pages > d.max_blocks_per_seq) return PKV_ERR_RANGE;
+  int chunk_tiles = 0;
+  const int chunks = prefix_chunks(d, a.num_tokens, a.shared_prefix_pages, &chunk_tiles);
   const WorkspaceLayout L =
-      workspace_layout(a.num_tokens, d.num_kv_heads * nsub, nwarps, GH, max_tiles);
+      workspace_layout(a.num_tokens, d.num_kv_heads * nsub, nwarps, GH, max_tiles,
+                       prefix_records(d, a.num_tokens, a.shared_prefix_pages));
   if (a.workspace_bytes < L.total) return PKV_ERR_WORKSPACE;
   if (a.num_tokens == 0 || a.num_seqs == 0) return PKV_OK;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
@@ -758,6 +925,10 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   const int split_max_q = prefill ? simt_max_q() : INT_MAX;
   if (prefill) {
     if (int e = launch_prefill(ctx, a, ws + L.tiles, split_max_q, max_tiles)) return e;
+  }
+  if (a.shared_prefix_pages > 0) {
+    if (int e = launch_prefix(ctx, a, reinterpret_cast<float*>(ws + L.prefix), chunks, chunk_tiles))
+      return e;
   }
 
   DecodeParams dp{};
@@ -783,6 +954,9 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   dp.nwarps = nwarps;
   dp.qscale = a.scale * 1.4426950408889634f;
   dp.epoch = next_epoch();
+  dp.np = a.shared_prefix_pages;
+  dp.chunks = chunks;
+  dp.prefix_part = reinterpret_cast<const float*>(ws + L.prefix);
 
   switch (GH) {
     case 1: return launch_decode<1>(ctx, dp);

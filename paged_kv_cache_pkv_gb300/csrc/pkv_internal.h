@@ -54,7 +54,7 @@ struct AttendArgs {
   const int32_t* block_tables;
   const int32_t* seq_lens;
   const int32_t* query_start_loc;
-  int32_t num_seqs, num_tokens, max_query_len;
+  int32_t num_seqs, num_tokens, max_query_len, shared_prefix_pages;
   float scale;
   uint16_t* out;
   void* workspace;
@@ -64,7 +64,7 @@ struct AttendArgs {
 
 // Workspace bytes for a batch on the current device.
 size_t attend_workspace_bytes(const DeviceInfo& dev, const pkv_desc& d, int32_t num_seqs,
-                              int32_t num_tokens);
+                              int32_t num_tokens, int32_t shared_prefix_pages);
 int launch_attend(const LaunchCtx& ctx, const AttendArgs& a);
 
 // Resident CTAs per SM of the decode kernel variant (occupancy query).
@@ -76,5 +76,10 @@ int prefill_max_tiles(const pkv_desc& d, int32_t num_seqs, int32_t num_tokens);
 // rows; `scratch` is the workspace's tile area.
 int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, void* scratch, int split_max_q,
                    int max_tiles);
+// Shared-prefix pass: key chunks of the prefix and tiles per chunk.
+int prefix_chunks(const pkv_desc& d, int32_t num_tokens, int32_t prefix_pages, int* chunk_tiles);
+// Every query row against the shared prefix pages -> partial records.
+int launch_prefix(const LaunchCtx& ctx, const AttendArgs& a, float* records, int chunks,
+                  int chunk_tiles);
 
 }  // namespace pkv

@@ -78,6 +78,10 @@ struct PrefillParams {
   unsigned* status;
   int32_t B, T, Hkv, Hq, G, TM, max_blocks, num_blocks, split_max_q;
   float qscale;  // scale * log2(e)
+  // shared-prefix pass: attend query rows to the first prefix_pages pages
+  // (common to every block-table row) in chunks of chunk_tiles key tiles
+  int32_t prefix_pages, chunk_tiles, chunks;
+  float* prefix_part;  // [T][Hq][chunks] records of kPrefixRec floats
 };
 
 // ---------------------------------------------------------------------------
@@ -205,6 +209,10 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
 // ---------------------------------------------------------------------------
 // kernel
 // ---------------------------------------------------------------------------
+// PREFIX = false: chunked prefill (bottom-right causal, normalised output).
+// PREFIX = true: every query row against the shared prefix keys, written as
+// log-sum-exp partial records that the split-KV kernel merges.
+template <bool PREFIX>
 __global__ void __launch_bounds__(kPfThreads, 1)
     pkv_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -232,18 +240,32 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = blockIdx.x;  // kv head; blockIdx.y = tile (real tiles dispatch first)
 
-  // ---- plan: which (sequence, first query token) this CTA's tile is --------
-  {
+  // ---- plan: this CTA's query rows and key window ----------------------------
+  int b = -1, t0 = 0, q_tok0 = 0, kbeg = 0, nkv = 0, key_end = 0, n = 0, L = 0;
+  const int32_t* bt_row = p.block_tables;  // shared prefix: any row; row 0
+  if constexpr (PREFIX) {
+    const int qtiles = (p.T + p.TM - 1) / p.TM;
+    const int i = int(blockIdx.y);
+    if (i >= qtiles * p.chunks) return;
+    const int qt = i / p.chunks, c = i - qt * p.chunks;
+    const int ntiles = (p.prefix_pages * kPage + kPfKeys - 1) / kPfKeys;
+    q_tok0 = qt * p.TM;
+    kbeg = c * p.chunk_tiles;
+    nkv = min(p.chunk_tiles, ntiles - kbeg);
+    key_end = p.prefix_pages * kPage;
+    b = c;  // chunk index (record slot)
+    if (nkv <= 0) return;
+  } else {
     const int per = (p.B + kPfThreads - 1) / kPfThreads;
     const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
     int local = 0;
-    for (int b = b0; b < b1; ++b) {
-      const int q0 = __ldg(p.qsl + b), q1 = __ldg(p.qsl + b + 1), L = __ldg(p.seq_lens + b);
-      const int n = q1 - q0;
-      const bool bad = q0 < 0 || n < 0 || q1 > p.T || n > L || L < 0 ||
-                       (L + kPage - 1) / kPage > p.max_blocks || (b == 0 && q0 != 0);
-      const int tiles = (!bad && n > p.split_max_q) ? (n + p.TM - 1) / p.TM : 0;
-      s_scan[b] = tiles;
+    for (int bb = b0; bb < b1; ++bb) {
+      const int qq0 = __ldg(p.qsl + bb), q1 = __ldg(p.qsl + bb + 1), LL = __ldg(p.seq_lens + bb);
+      const int nn = q1 - qq0;
+      const bool bad = qq0 < 0 || nn < 0 || q1 > p.T || nn > LL || LL < 0 ||
+                       (LL + kPage - 1) / kPage > p.max_blocks || (bb == 0 && qq0 != 0);
+      const int tiles = (!bad && nn > p.split_max_q) ? (nn + p.TM - 1) / p.TM : 0;
+      s_scan[bb] = tiles;
       local += tiles;
     }
     int incl = local;
@@ -261,9 +283,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       total += s_wsum[x];
     }
     int run = base + incl - local;
-    for (int b = b0; b < b1; ++b) {
-      const int c = s_scan[b];
-      s_scan[b] = run;
+    for (int bb = b0; bb < b1; ++bb) {
+      const int c = s_scan[bb];
+      s_scan[bb] = run;
       run += c;
     }
     if (tid == 0) s_scan[p.B] = total;
@@ -271,30 +293,33 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (tid == 0) {
       // heavier tiles (later sequences, later query blocks) first
       const int i = total - 1 - int(blockIdx.y);
-      int b = -1, t0 = 0;
+      int bb = -1, tt = 0;
       if (i >= 0) {
         int lo = 0, hi = p.B;  // last b with s_scan[b] <= i
         while (hi - lo > 1) {
           const int mid = (lo + hi) >> 1;
           if (s_scan[mid] <= i) lo = mid; else hi = mid;
         }
-        b = lo;
-        t0 = (i - s_scan[lo]) * p.TM;
+        bb = lo;
+        tt = (i - s_scan[lo]) * p.TM;
       }
-      s_info[0] = b;
-      s_info[1] = t0;
+      s_info[0] = bb;
+      s_info[1] = tt;
     }
     __syncthreads();
+    b = s_info[0];
+    if (b < 0) return;  // no tile for this CTA (before any TMEM is taken)
+    t0 = s_info[1];
+    const int q0 = __ldg(p.qsl + b);
+    n = __ldg(p.qsl + b + 1) - q0;
+    L = __ldg(p.seq_lens + b);
+    q_tok0 = q0 + t0;
+    key_end = L;
+    const int max_pos = L - n + min(n, t0 + p.TM) - 1;
+    nkv = max_pos / kPfKeys + 1;
+    bt_row = p.block_tables + int64_t(b) * p.max_blocks;
   }
-  const int b = s_info[0];
-  if (b < 0) return;  // no tile for this CTA (before any TMEM is taken)
-  const int t0 = s_info[1];
-  const int q0 = __ldg(p.qsl + b);
-  const int n = __ldg(p.qsl + b + 1) - q0;
-  const int L = __ldg(p.seq_lens + b);
-  const int npages = (L + kPage - 1) / kPage;
-  const int max_pos = L - n + min(n, t0 + p.TM) - 1;
-  const int nkv = max_pos / kPfKeys + 1;
+  const int npages = (key_end + kPage - 1) / kPage;
 
   // ---- barriers and TMEM -----------------------------------------------------
   if (tid == 0) {
@@ -324,11 +349,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int role = warp - kPfSoftmaxThreads / 32;  // 0: K loads, 1: V loads, 2: MMA; < 0 softmax
 
   // block ids of the 8 pages of K/V tile kt (pages past the sequence: -1)
-  auto page_ids = [&](int kt, int (&bids)[kPfPagesPerTile]) {
+  auto page_ids = [&](int kt, int (&bids)[kPfPagesPerTile]) {  // kt: tile of this CTA's window
 #pragma unroll
     for (int j = 0; j < kPfPagesPerTile; ++j) {
-      const int pi = kt * kPfPagesPerTile + j;
-      bids[j] = pi < npages ? __ldg(p.block_tables + int64_t(b) * p.max_blocks + pi) : -1;
+      const int pi = (kbeg + kt) * kPfPagesPerTile + j;
+      bids[j] = pi < npages ? __ldg(bt_row + pi) : -1;
     }
   };
   auto load_tile = [&](const CUtensorMap* map, uint8_t* base, uint64_t* bar, const int (&bids)[kPfPagesPerTile]) {
@@ -363,7 +388,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
         mbar_arrive_expect_tx(bar_q, 2 * kHalfTile);
         for (int h = 0; h < 2; ++h)
-          tma_load_3d(sQ + h * kHalfTile, &tm_q, h * 64, g * p.G, q0 + t0, bar_q);
+          tma_load_3d(sQ + h * kHalfTile, &tm_q, h * 64, g * p.G, q_tok0, bar_q);
       }
       int ids[kPfPagesPerTile], next[kPfPagesPerTile];
       page_ids(0, ids);
@@ -434,8 +459,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int r = tid & 127;  // query row == TMEM lane
     const int ch = tid >> 7;  // which 64 of the 128 score columns
     const int t_rel = r / p.G;
-    const bool row_valid = t0 + t_rel < n;
-    const int pos = row_valid ? L - n + t0 + t_rel : L - 1;
+    // keys visible to this row: prefix pass sees the whole window
+    const bool row_valid = PREFIX ? q_tok0 + t_rel < p.T : t0 + t_rel < n;
+    const int pos = PREFIX ? key_end - 1 : (row_valid ? L - n + t0 + t_rel : L - 1);
     float m = -INFINITY, l = 0.f;  // running max (same in both threads of a row), half row sum
     float* s_red = reinterpret_cast<float*>(sm + kOffMisc + 256);  // [2][128] exchange
     bool ok = true;
@@ -446,7 +472,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (it >= 2) ok = ok && mbar_wait(bar_o + buf, ph ^ 1);
       tc_fence_after();
       // ---- this thread's 64 columns of row r ----
-      const int kbase = it * kPfKeys + ch * 64;
+      const int kbase = (kbeg + it) * kPfKeys + ch * 64;
       // no masking in this half tile for any row of the warp: the pass below
       // runs warp-collective TMEM loads, so the choice must be warp-uniform
       const bool full = __all_sync(0xffffffffu, kbase + 63 <= pos);
@@ -541,9 +567,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       // keys past the sequence end: zero their V rows (after V landed) so
       // stale pool contents cannot leak through P = 0
-      if ((it + 1) * kPfKeys > L) {
+      if ((kbeg + it + 1) * kPfKeys > key_end) {
         ok = mbar_wait(bar_v + buf, ph) && ok;
-        if (it * kPfKeys + r >= L) {
+        if ((kbeg + it) * kPfKeys + r >= key_end) {
           uint4* vrow = reinterpret_cast<uint4*>(sV + (buf * 2 + ch) * kHalfTile + r * 128);
 #pragma unroll
           for (int q = 0; q < 8; ++q) vrow[q] = make_uint4(0, 0, 0, 0);
@@ -558,23 +584,47 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     s_red[ch * 128 + r] = l;
     named_sync(1, kPfSoftmaxThreads);
     tc_fence_after();
-    const float inv = 1.f / (s_red[r] + s_red[128 + r]);
-    uint16_t* orow = p.out + (size_t(q0 + t0 + t_rel) * p.Hq + g * p.G + (r % p.G)) * kHeadDim + ch * 64;
+    const float lsum = s_red[r] + s_red[128 + r];
+    if constexpr (PREFIX) {
+      // partial record: o (unnormalised, 128 floats), running max m, sum l
+      float* rec = p.prefix_part +
+                   ((size_t(q_tok0 + t_rel) * p.Hq + g * p.G + (r % p.G)) * p.chunks + b) * kPrefixRec;
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      uint32_t ov[32];
-      tmem_ld32(tmem_o + lane_off + ch * 64 + c * 32, ov);
-      tmem_wait_ld();
-      if (row_valid && ok) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+      for (int c = 0; c < 2; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tmem_o + lane_off + ch * 64 + c * 32, ov);
+        tmem_wait_ld();
+        if (row_valid && ok) {
+          float4* dst = reinterpret_cast<float4*>(rec + ch * 64 + c * 32);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t w4[4];
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(ov[4 * q]), __uint_as_float(ov[4 * q + 1]),
+                                 __uint_as_float(ov[4 * q + 2]), __uint_as_float(ov[4 * q + 3]));
+        }
+      }
+      if (row_valid && ok && ch == 0) {
+        rec[128] = m;
+        rec[129] = lsum;
+      }
+    } else {
+      const float inv = 1.f / lsum;
+      uint16_t* orow = p.out + (size_t(q_tok0 + t_rel) * p.Hq + g * p.G + (r % p.G)) * kHeadDim + ch * 64;
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w4[e] = pack_bf16x2(__uint_as_float(ov[8 * q + 2 * e]) * inv,
-                                __uint_as_float(ov[8 * q + 2 * e + 1]) * inv);
-          dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      for (int c = 0; c < 2; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tmem_o + lane_off + ch * 64 + c * 32, ov);
+        tmem_wait_ld();
+        if (row_valid && ok) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w4[e] = pack_bf16x2(__uint_as_float(ov[8 * q + 2 * e]) * inv,
+                                  __uint_as_float(ov[8 * q + 2 * e + 1]) * inv);
+            dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
         }
       }
     }
@@ -630,34 +680,41 @@ int prefill_max_tiles(const pkv_desc& d, int32_t num_seqs, int32_t num_tokens) {
   return (num_tokens + tm - 1) / tm + num_seqs;
 }
 
-int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, void* /*scratch*/, int split_max_q,
-                   int max_tiles) {
-  const pkv_desc& d = a.desc;
-  const int G = d.num_q_heads / d.num_kv_heads;
-  static bool attr_set[64] = {};
-  if (ctx.dev->device >= 0 && ctx.dev->device < 64 && !attr_set[ctx.dev->device]) {
-    if (cudaFuncSetAttribute(pkv_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <bool PREFIX>
+static int ensure_prefill_attr(int device) {
+  static bool done[2][64] = {};
+  if (device < 0 || device >= 64) return PKV_ERR_DEVICE;
+  if (!done[PREFIX][device]) {
+    if (cudaFuncSetAttribute(pkv_prefill_kernel<PREFIX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kPfSmemBytes)) != cudaSuccess) {
       cudaGetLastError();
       return PKV_ERR_LAUNCH;
     }
-    attr_set[ctx.dev->device] = true;
+    done[PREFIX][device] = true;
   }
-  CUtensorMap tq, tk, tv;
+  return PKV_OK;
+}
+
+static int make_maps(const AttendArgs& a, CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv) {
+  const pkv_desc& d = a.desc;
+  const int G = d.num_q_heads / d.num_kv_heads;
   {
     const cuuint64_t dims[3] = {cuuint64_t(kHeadDim), cuuint64_t(d.num_q_heads), cuuint64_t(a.num_tokens)};
     const cuuint64_t strides[2] = {cuuint64_t(kHeadDim) * 2, cuuint64_t(d.num_q_heads) * kHeadDim * 2};
     const cuuint32_t box[3] = {64, cuuint32_t(G), cuuint32_t(tile_tokens(d))};
-    if (!encode(&tq, a.q, 3, dims, strides, box)) return PKV_ERR_LAUNCH;
+    if (!encode(tq, a.q, 3, dims, strides, box)) return PKV_ERR_LAUNCH;
   }
-  {
-    const cuuint64_t rows = cuuint64_t(d.num_blocks) * d.num_kv_heads * kPage;
-    const cuuint64_t dims[2] = {cuuint64_t(kHeadDim), rows};
-    const cuuint64_t strides[1] = {cuuint64_t(kHeadDim) * 2};
-    const cuuint32_t box[2] = {64, cuuint32_t(kPage)};
-    if (!encode(&tk, a.k_cache, 2, dims, strides, box)) return PKV_ERR_LAUNCH;
-    if (!encode(&tv, a.v_cache, 2, dims, strides, box)) return PKV_ERR_LAUNCH;
-  }
+  const cuuint64_t rows = cuuint64_t(d.num_blocks) * d.num_kv_heads * kPage;
+  const cuuint64_t dims[2] = {cuuint64_t(kHeadDim), rows};
+  const cuuint64_t strides[1] = {cuuint64_t(kHeadDim) * 2};
+  const cuuint32_t box[2] = {64, cuuint32_t(kPage)};
+  if (!encode(tk, a.k_cache, 2, dims, strides, box)) return PKV_ERR_LAUNCH;
+  if (!encode(tv, a.v_cache, 2, dims, strides, box)) return PKV_ERR_LAUNCH;
+  return PKV_OK;
+}
+
+static PrefillParams make_params(const LaunchCtx& ctx, const AttendArgs& a, int split_max_q) {
+  const pkv_desc& d = a.desc;
   PrefillParams pp{};
   pp.block_tables = a.block_tables;
   pp.seq_lens = a.seq_lens;
@@ -668,15 +725,57 @@ int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, void* /*scratch*/,
   pp.T = a.num_tokens;
   pp.Hkv = d.num_kv_heads;
   pp.Hq = d.num_q_heads;
-  pp.G = G;
+  pp.G = d.num_q_heads / d.num_kv_heads;
   pp.TM = tile_tokens(d);
   pp.max_blocks = d.max_blocks_per_seq;
   pp.num_blocks = d.num_blocks;
   pp.split_max_q = split_max_q;
   pp.qscale = a.scale * 1.4426950408889634f;
+  return pp;
+}
+
+int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, void* /*scratch*/, int split_max_q,
+                   int max_tiles) {
+  if (int e = ensure_prefill_attr<false>(ctx.dev->device)) return e;
+  CUtensorMap tq, tk, tv;
+  if (int e = make_maps(a, &tq, &tk, &tv)) return e;
+  const PrefillParams pp = make_params(ctx, a, split_max_q);
   TraceScope ts(ctx.stream, PKV_K_PREFILL);
-  pkv_prefill_kernel<<<dim3(d.num_kv_heads, max_tiles), kPfThreads, kPfSmemBytes, ctx.stream>>>(
-      tq, tk, tv, pp);
+  pkv_prefill_kernel<false><<<dim3(a.desc.num_kv_heads, max_tiles), kPfThreads, kPfSmemBytes,
+                              ctx.stream>>>(tq, tk, tv, pp);
+  return ts.done();
+}
+
+int prefix_chunks(const pkv_desc& d, int32_t num_tokens, int32_t prefix_pages, int* chunk_tiles) {
+  if (prefix_pages <= 0 || num_tokens <= 0) {
+    *chunk_tiles = 0;
+    return 0;
+  }
+  const int tm = tile_tokens(d);
+  const int qtiles = (num_tokens + tm - 1) / tm;
+  const int ntiles = (prefix_pages * kPage + kPfKeys - 1) / kPfKeys;
+  // split the prefix keys until the pass has about one CTA per SM (152), at
+  // most 16 chunks (the split-KV merge holds one chunk per lane of a half warp)
+  const int want = min(16, max(1, (152 + qtiles * d.num_kv_heads - 1) / (qtiles * d.num_kv_heads)));
+  const int per = max(1, (ntiles + want - 1) / want);
+  *chunk_tiles = per;
+  return (ntiles + per - 1) / per;
+}
+
+int launch_prefix(const LaunchCtx& ctx, const AttendArgs& a, float* records, int chunks,
+                  int chunk_tiles) {
+  if (int e = ensure_prefill_attr<true>(ctx.dev->device)) return e;
+  CUtensorMap tq, tk, tv;
+  if (int e = make_maps(a, &tq, &tk, &tv)) return e;
+  PrefillParams pp = make_params(ctx, a, 0);
+  pp.prefix_pages = a.shared_prefix_pages;
+  pp.chunk_tiles = chunk_tiles;
+  pp.chunks = chunks;
+  pp.prefix_part = records;
+  const int qtiles = (a.num_tokens + pp.TM - 1) / pp.TM;
+  TraceScope ts(ctx.stream, PKV_K_PREFILL);
+  pkv_prefill_kernel<true><<<dim3(a.desc.num_kv_heads, qtiles * chunks), kPfThreads, kPfSmemBytes,
+                             ctx.stream>>>(tq, tk, tv, pp);
   return ts.done();
 }
 

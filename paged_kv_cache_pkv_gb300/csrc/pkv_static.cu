@@ -43,17 +43,19 @@ extern "C" PKV_API int pkv_attend_static(const pkv_bf16* q, const pkv_bf16* k_ca
                                          const pkv_bf16* v_cache, const int32_t* block_tables,
                                          const int32_t* seq_lens, const int32_t* query_start_loc,
                                          int32_t num_seqs, int32_t num_tokens,
-                                         int32_t max_query_len, float scale, pkv_bf16* out,
-                                         const pkv_desc* desc, pkv_stream_t stream) {
+                                         int32_t max_query_len, int32_t shared_prefix_pages,
+                                         float scale, pkv_bf16* out, const pkv_desc* desc,
+                                         pkv_stream_t stream) {
   using namespace pkv;
   size_t need = 0;
-  if (int e = pkv_attend_workspace_size(desc, num_seqs, num_tokens, &need)) return e;
+  if (int e = pkv_attend_workspace_size(desc, num_seqs, num_tokens, shared_prefix_pages, &need))
+    return e;
   if (need > PKV_STATIC_SCRATCH_BYTES) return PKV_ERR_SCRATCH;
   int device = -1;
   if (cudaGetDevice(&device) != cudaSuccess) return PKV_ERR_DEVICE;
   void* scratch = nullptr;
   if (int e = static_scratch(device, &scratch)) return e;
   return pkv_attend(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, num_seqs,
-                    num_tokens, max_query_len, scale, out, scratch, PKV_STATIC_SCRATCH_BYTES, desc,
-                    stream);
+                    num_tokens, max_query_len, shared_prefix_pages, scale, out, scratch,
+                    PKV_STATIC_SCRATCH_BYTES, desc, stream);
 }

@@ -53,7 +53,7 @@ def _write(lib, desc, **ptrs):
 def _attend(lib, desc, B=4, T=4, **ptrs):
     p = dict(q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, sl=FAKE, qsl=FAKE, out=FAKE, ws=FAKE)
     p.update(ptrs)
-    return lib.pkv_attend(p["q"], p["kc"], p["vc"], p["bt"], p["sl"], p["qsl"], B, T, 0, 0.1,
+    return lib.pkv_attend(p["q"], p["kc"], p["vc"], p["bt"], p["sl"], p["qsl"], B, T, 0, 0, 0.1,
                           p["out"], p["ws"], 1 << 20, ctypes.byref(desc), None)
 
 
@@ -66,7 +66,7 @@ def test_bad_geometry_rejected(pkvlib, bad, code):
     assert _write(pkvlib, _desc(**bad)) == code
     assert _attend(pkvlib, _desc(**bad)) == code
     n = ctypes.c_size_t(0)
-    assert pkvlib.pkv_attend_workspace_size(ctypes.byref(_desc(**bad)), 4, 4, ctypes.byref(n)) == code
+    assert pkvlib.pkv_attend_workspace_size(ctypes.byref(_desc(**bad)), 4, 4, 0, ctypes.byref(n)) == code
 
 
 def test_null_and_misaligned_pointers_rejected(pkvlib):
@@ -80,7 +80,7 @@ def test_null_and_misaligned_pointers_rejected(pkvlib):
     assert _attend(pkvlib, d, ws=ctypes.c_void_p((1 << 20) + 128)) == -2
     assert _attend(pkvlib, d, B=-1) == -4
     assert pkvlib.pkv_write(FAKE, FAKE, FAKE, -1, FAKE, FAKE, ctypes.byref(d), None) == -4
-    assert pkvlib.pkv_attend(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 0, 0.1, FAKE, FAKE, 1 << 20,
+    assert pkvlib.pkv_attend(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 0, 0, 0.1, FAKE, FAKE, 1 << 20,
                              None, None) == -1
 
 

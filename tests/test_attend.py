@@ -215,3 +215,63 @@ def test_prefill_chunks_all_rows(pkvlib, hq, hkv, L, n):
     assert counts["prefill"] == 1
     k_ref, v_ref = oracle_write(b)
     compare(out, oracle_attend(b, k_ref, v_ref), what=f"prefill {hq}/{hkv} L={L} n={n}")
+
+
+def _cascade(batch, prefix_pages, max_query_len=0):
+    meta = to_device(batch)
+    kc, vc = batch.k_cache.clone(), batch.v_cache.clone()
+    pkv.write(batch.k_new, batch.v_new, meta["slot_mapping"], kc, vc)
+    out = pkv.attend(batch.q, kc, vc, meta["block_tables"], meta["seq_lens"], meta["query_start_loc"],
+                     batch.scale, max_query_len=max_query_len, shared_prefix_pages=prefix_pages)
+    torch.cuda.synchronize()
+    return out
+
+
+def test_cascade_prefix_shared_workload(pkvlib):
+    """Config 4: 128 sequences on one 2048-token prefix, cascade vs oracle."""
+    b = workload(4, device="cuda")
+    out = _cascade(b, b.info["shared_prefix_pages"], max_query_len=1)
+    assert pkv.get_last_error() == 0
+    k_ref, v_ref = oracle_write(b)
+    compare(out, oracle_attend(b, k_ref, v_ref), what="cascade cfg4")
+
+
+@pytest.mark.parametrize("hq,hkv,prefix,suffixes", [
+    (32, 8, 80, [1, 17, 100, 16]),        # prefix of 5 pages: one partial key tile
+    (16, 2, 1600, [3, 250, 33]),          # several key chunks of the prefix
+    (8, 8, 256, [40, 1, 2]),              # one query head per kv head
+    (64, 8, 512, [70, 5]),                # 8 query heads per kv head (two head groups)
+    (8, 4, 16, [1, 2, 3, 4, 5]),          # one-page prefix, tiny suffixes
+])
+def test_cascade_small(pkvlib, hq, hkv, prefix, suffixes):
+    lens = [prefix + s for s in suffixes]
+    b = make_batch(lens, [1] * len(lens), hq, hkv, seed=prefix + len(suffixes), device="cuda",
+                   pool_factor=1.0, shared_prefix_tokens=prefix)
+    out = _cascade(b, prefix // 16, max_query_len=1)
+    assert pkv.get_last_error() == 0
+    k_ref, v_ref = oracle_write(b)
+    compare(out, oracle_attend(b, k_ref, v_ref), what=f"cascade {hq}/{hkv} prefix {prefix}")
+
+
+def test_cascade_with_prefill_chunk_and_speculative_rows(pkvlib):
+    """A shared prefix with decode rows, short multi-row chunks (split-KV) and
+    a long chunk (tensor-core prefill, which reads the prefix itself)."""
+    prefix = 512
+    b = make_batch([prefix + 30, prefix + 200, prefix + 64, prefix + 9], [1, 40, 3, 9], 32, 8, seed=77,
+                   device="cuda", pool_factor=1.0, shared_prefix_tokens=prefix)
+    out = _cascade(b, prefix // 16)
+    assert pkv.get_last_error() == 0
+    k_ref, v_ref = oracle_write(b)
+    compare(out, oracle_attend(b, k_ref, v_ref), what="cascade mixed")
+
+
+def test_cascade_row_without_own_key_is_flagged(pkvlib):
+    b = make_batch([160, 200], [1, 1], 8, 2, seed=78, device="cuda", pool_factor=1.0,
+                   shared_prefix_tokens=144)
+    pkv.get_last_error()
+    meta = to_device(b)
+    kc, vc = b.k_cache.clone(), b.v_cache.clone()
+    # claim a 10-page prefix: sequence 0 (160 tokens) has no key past it
+    pkv.attend(b.q, kc, vc, meta["block_tables"], meta["seq_lens"], meta["query_start_loc"], b.scale,
+               max_query_len=1, shared_prefix_pages=10)
+    assert pkv.get_last_error() & pkv.STATUS_BAD_QUERY

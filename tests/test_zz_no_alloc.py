@@ -30,7 +30,7 @@ def _static_call(lib, b, meta, kc, vc, out):
     return lib.pkv_attend_static(
         ctypes.c_void_p(b.q.data_ptr()), ctypes.c_void_p(kc.data_ptr()), ctypes.c_void_p(vc.data_ptr()),
         ctypes.c_void_p(meta["block_tables"].data_ptr()), ctypes.c_void_p(meta["seq_lens"].data_ptr()),
-        ctypes.c_void_p(meta["query_start_loc"].data_ptr()), b.B, b.T, 0, b.scale,
+        ctypes.c_void_p(meta["query_start_loc"].data_ptr()), b.B, b.T, 0, 0, b.scale,
         ctypes.c_void_p(out.data_ptr()), ctypes.byref(desc), stream)
 
 
@@ -67,10 +67,10 @@ def test_static_scratch_rejects_oversized_batch(pkvlib):
     desc = pkv.Desc(1024, 16, 8, 32, 128, 4)
     need = ctypes.c_size_t(0)
     T = 1 << 20  # per-row plan arrays alone exceed the fixed scratch
-    assert pkvlib.pkv_attend_workspace_size(ctypes.byref(desc), 4, T, ctypes.byref(need)) == 0
+    assert pkvlib.pkv_attend_workspace_size(ctypes.byref(desc), 4, T, 0, ctypes.byref(need)) == 0
     assert need.value > (8 << 20)
     fake = ctypes.c_void_p(1 << 20)
     before = pkvlib.pkv_launch_count()
-    assert pkvlib.pkv_attend_static(fake, fake, fake, fake, fake, fake, 4, T, 0, 0.1, fake,
+    assert pkvlib.pkv_attend_static(fake, fake, fake, fake, fake, fake, 4, T, 0, 0, 0.1, fake,
                                     ctypes.byref(desc), None) == -9
     assert pkvlib.pkv_launch_count() == before
