@@ -74,6 +74,7 @@ typedef struct CUevent_st* pkv_event_t;    /* same handle as cudaEvent_t    */
 #define PKV_ERR_DEVICE     (-7)  /* current device is not an sm_103 GPU          */
 #define PKV_ERR_STATE      (-8)  /* misuse of the trace API                      */
 #define PKV_ERR_SCRATCH    (-9)  /* batch too large for pkv_attend_static        */
+#define PKV_ERR_NOSPACE   (-10)  /* page pool: not enough free pages             */
 
 /* ---- device status bits (pkv_get_last_error) ------------------------------- */
 #define PKV_STATUS_BAD_SLOT   0x1u  /* slot_mapping entry beyond the pool: skipped */
@@ -201,6 +202,60 @@ PKV_API int pkv_attend_static(const pkv_bf16* q, const pkv_bf16* k_cache,
                               int32_t max_query_len, int32_t shared_prefix_pages,
                               float scale, pkv_bf16* out, const pkv_desc* desc,
                               pkv_stream_t stream);
+
+/* ---- page pool (host side) ------------------------------------------------ */
+/* The engine reserves num_gpu_blocks pages of block_size tokens (vLLM notes
+ * "EngineCoreClient ...", "Flujo de datos"); the native coordinator owns the
+ * retained pages with a single writer (TensorRT Edge-LLM "HTTP Inference
+ * Server Architecture", "Request Lifecycle"); cached prefix pages are reused
+ * by later requests and the usage fraction is exported as a gauge (llm-d
+ * blog, prefix producers; vllm:kv_cache_usage_perc).  pkv_pool hands out
+ * page ids for block tables, counts references to pages shared by several
+ * sequences, and gives a sequence a private copy of a shared page before it
+ * writes into it.  Calls are serialised by an internal mutex.  Page ids are
+ * indices into the pools of pkv_desc (num_blocks must match). */
+typedef struct pkv_pool pkv_pool;
+PKV_API int pkv_pool_create(int32_t num_blocks, pkv_pool** out);
+PKV_API int pkv_pool_destroy(pkv_pool* pool);
+/* n fresh pages (reference count 1) into pages[0..n); all or nothing:
+ * PKV_ERR_NOSPACE when fewer than n are free.  Recently freed pages first. */
+PKV_API int pkv_pool_alloc(pkv_pool* pool, int32_t n, int32_t* pages);
+/* One more reference to each listed page (a sequence reusing a prefix). */
+PKV_API int pkv_pool_retain(pkv_pool* pool, const int32_t* pages, int32_t n);
+/* Drop one reference per listed page; a page is freed at zero.  Releasing a
+ * free page (or more references than held) is PKV_ERR_STATE and changes
+ * nothing. */
+PKV_API int pkv_pool_release(pkv_pool* pool, const int32_t* pages, int32_t n);
+PKV_API int pkv_pool_refcount(pkv_pool* pool, int32_t page, int32_t* count);
+/* Pages in use and in the pool; usage = used / total. */
+PKV_API int pkv_pool_usage(pkv_pool* pool, int32_t* used, int32_t* total);
+/* Copy-on-write: if `page` has one reference it is already private and is
+ * returned in *new_page.  Otherwise a fresh page is taken, rows [0, rows) of
+ * every kv head of `page` are copied into it (K and V, device, on `stream`),
+ * the caller's reference moves to the fresh page and *new_page names it.
+ * The caller then points its block table at *new_page. */
+PKV_API int pkv_pool_make_writable(pkv_pool* pool, int32_t page, int32_t rows,
+                                   pkv_bf16* k_cache, pkv_bf16* v_cache,
+                                   const pkv_desc* desc, pkv_stream_t stream,
+                                   int32_t* new_page);
+
+/* ---- page transfer -------------------------------------------------------- */
+/* Disaggregated serving moves a request's KV pages from the prefill engine to
+ * the decode engine (llm-d blog, P/D disaggregation paragraphs; there over
+ * RDMA).  These calls are its single-GPU part: copy whole pages between the
+ * pools and a contiguous buffer laid out [n][2 (K, V)][num_kv_heads][16][128]
+ * bf16, i.e. each listed page's K rows then its V rows.  The buffer may be
+ * device memory or pinned host memory the GPU can reach (on GB300 pinned
+ * host memory is read and written directly over NVLink-C2C).
+ *   pages [n] int32, device (readable by the device): page ids; an id
+ *   outside [0, num_blocks) is skipped and flags PKV_STATUS_BAD_BLOCK.
+ * Stream-ordered; bit-exact. */
+PKV_API int pkv_export_pages(const pkv_bf16* k_cache, const pkv_bf16* v_cache,
+                             const int32_t* pages, int32_t n, pkv_bf16* dst,
+                             const pkv_desc* desc, pkv_stream_t stream);
+PKV_API int pkv_import_pages(const pkv_bf16* src, const int32_t* pages, int32_t n,
+                             pkv_bf16* k_cache, pkv_bf16* v_cache,
+                             const pkv_desc* desc, pkv_stream_t stream);
 
 /* Wait for `stream`, then read and clear the current device's status word
  * (PKV_STATUS_* bits) into *flags. */

@@ -49,6 +49,8 @@ import numpy as np
 __all__ = [
     "bf16_to_f64",
     "write",
+    "export_pages",
+    "import_pages",
     "gather",
     "attend",
     "attend_one",
@@ -91,6 +93,26 @@ def write(k_new, v_new, slot_mapping, k_cache, v_cache, page_size):
             raise IndexError(f"slot {int(s)} of token {t} is outside the pool")
         k_out[page, :, row, :] = k_new[t]
         v_out[page, :, row, :] = v_new[t]
+    return k_out, v_out
+
+
+def export_pages(k_cache, v_cache, pages):
+    """Whole pages in transfer order: [n, 2 (K, V), Hkv, P, D] bit patterns.
+
+    A disaggregated prefill engine hands a request's KV pages to the decode
+    engine (llm-d blog, P/D disaggregation); this is the content moved.
+    """
+    pages = np.asarray(pages, dtype=np.int64)
+    return np.stack([np.asarray(k_cache)[pages], np.asarray(v_cache)[pages]], axis=1)
+
+
+def import_pages(buf, pages, k_cache, v_cache):
+    """Inverse of export_pages: returns new (k_cache, v_cache) with the
+    listed pages replaced by the buffer's content (later duplicates win)."""
+    k_out, v_out = np.array(k_cache, copy=True), np.array(v_cache, copy=True)
+    for i, pg in enumerate(np.asarray(pages, dtype=np.int64)):
+        k_out[pg] = buf[i, 0]
+        v_out[pg] = buf[i, 1]
     return k_out, v_out
 
 

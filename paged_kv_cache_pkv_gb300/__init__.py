@@ -19,7 +19,8 @@ import torch
 
 __all__ = [
     "PkvError", "PkvUnavailable", "lib", "library_path", "Desc", "write", "attend",
-    "workspace_size", "get_last_error", "launch_count", "Trace", "KERNELS",
+    "workspace_size", "get_last_error", "launch_count", "Trace", "PagePool", "KERNELS",
+    "export_pages", "import_pages",
     "STATUS_BAD_SLOT", "STATUS_BAD_BLOCK", "STATUS_BAD_QUERY", "STATUS_TIMEOUT",
 ]
 
@@ -64,6 +65,17 @@ _SIGS = {
     "pkv_trace_read": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i64)]),
     "pkv_trace_reset": (ctypes.c_int, [_vp]),
     "pkv_trace_destroy": (ctypes.c_int, [_vp]),
+    "pkv_export_pages": (ctypes.c_int, [_vp, _vp, _vp, _i32, _vp, ctypes.POINTER(Desc), _vp]),
+    "pkv_import_pages": (ctypes.c_int, [_vp, _vp, _i32, _vp, _vp, ctypes.POINTER(Desc), _vp]),
+    "pkv_pool_create": (ctypes.c_int, [_i32, ctypes.POINTER(_vp)]),
+    "pkv_pool_destroy": (ctypes.c_int, [_vp]),
+    "pkv_pool_alloc": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_i32)]),
+    "pkv_pool_retain": (ctypes.c_int, [_vp, ctypes.POINTER(_i32), _i32]),
+    "pkv_pool_release": (ctypes.c_int, [_vp, ctypes.POINTER(_i32), _i32]),
+    "pkv_pool_refcount": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_i32)]),
+    "pkv_pool_usage": (ctypes.c_int, [_vp, ctypes.POINTER(_i32), ctypes.POINTER(_i32)]),
+    "pkv_pool_make_writable": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, ctypes.POINTER(Desc), _vp,
+                                              ctypes.POINTER(_i32)]),
 }
 
 _lib = None
@@ -190,6 +202,34 @@ def attend(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, 
     return out
 
 
+def export_pages(k_cache, v_cache, pages, out=None, stream=None):
+    """Copy whole pages into a contiguous buffer [n, 2, Hkv, 16, 128] bf16
+    (device or pinned host tensor); returns it."""
+    _need(pages, "pages", torch.int32, 1)
+    n = pages.shape[0]
+    if out is None:
+        out = torch.empty((n, 2) + tuple(k_cache.shape[1:]), dtype=torch.bfloat16, device=k_cache.device)
+    if out.dtype != torch.bfloat16 or not out.is_contiguous() or out.numel() != n * 2 * k_cache[0].numel():
+        raise ValueError("out must be a contiguous bf16 tensor of n * 2 pages")
+    desc = make_desc(k_cache, k_cache.shape[1], 1)
+    with torch.cuda.device(k_cache.device):
+        _check(lib().pkv_export_pages(_ptr(k_cache), _ptr(v_cache), _ptr(pages), n, _ptr(out),
+                                      ctypes.byref(desc), _stream(k_cache.device, stream)), "pkv_export_pages")
+    return out
+
+
+def import_pages(src, pages, k_cache, v_cache, stream=None):
+    """Copy a buffer written by export_pages into the listed pool pages."""
+    _need(pages, "pages", torch.int32, 1)
+    n = pages.shape[0]
+    if src.dtype != torch.bfloat16 or not src.is_contiguous() or src.numel() != n * 2 * k_cache[0].numel():
+        raise ValueError("src must be a contiguous bf16 tensor of n * 2 pages")
+    desc = make_desc(k_cache, k_cache.shape[1], 1)
+    with torch.cuda.device(k_cache.device):
+        _check(lib().pkv_import_pages(_ptr(src), _ptr(pages), n, _ptr(k_cache), _ptr(v_cache),
+                                      ctypes.byref(desc), _stream(k_cache.device, stream)), "pkv_import_pages")
+
+
 def get_last_error(device=None, stream=None):
     """Wait for the stream; read and clear the device status bits."""
     flags = ctypes.c_uint32(0)
@@ -201,6 +241,64 @@ def get_last_error(device=None, stream=None):
 
 def launch_count():
     return int(lib().pkv_launch_count())
+
+
+class PagePool:
+    """Host-side page allocator with reference counts (see pkv_pool_* in pkv.h)."""
+
+    def __init__(self, num_blocks):
+        h = ctypes.c_void_p()
+        _check(lib().pkv_pool_create(int(num_blocks), ctypes.byref(h)), "pkv_pool_create")
+        self._h, self.num_blocks = h, int(num_blocks)
+
+    @staticmethod
+    def _arr(pages):
+        pages = [int(x) for x in pages]
+        return (ctypes.c_int32 * max(1, len(pages)))(*pages), len(pages)
+
+    def alloc(self, n):
+        buf = (ctypes.c_int32 * max(1, n))()
+        _check(lib().pkv_pool_alloc(self._h, int(n), buf), "pkv_pool_alloc")
+        return list(buf)[:n]
+
+    def retain(self, pages):
+        a, n = self._arr(pages)
+        _check(lib().pkv_pool_retain(self._h, a, n), "pkv_pool_retain")
+
+    def release(self, pages):
+        a, n = self._arr(pages)
+        _check(lib().pkv_pool_release(self._h, a, n), "pkv_pool_release")
+
+    def refcount(self, page):
+        c = ctypes.c_int32(0)
+        _check(lib().pkv_pool_refcount(self._h, int(page), ctypes.byref(c)), "pkv_pool_refcount")
+        return c.value
+
+    def usage(self):
+        u, t = ctypes.c_int32(0), ctypes.c_int32(0)
+        _check(lib().pkv_pool_usage(self._h, ctypes.byref(u), ctypes.byref(t)), "pkv_pool_usage")
+        return u.value, t.value
+
+    def make_writable(self, page, rows, k_cache, v_cache, stream=None):
+        """Private copy of a shared page (copy-on-write); returns the page to write."""
+        desc = make_desc(k_cache, k_cache.shape[1], 1)
+        out = ctypes.c_int32(-1)
+        with torch.cuda.device(k_cache.device):
+            _check(lib().pkv_pool_make_writable(self._h, int(page), int(rows), _ptr(k_cache), _ptr(v_cache),
+                                                ctypes.byref(desc), _stream(k_cache.device, stream),
+                                                ctypes.byref(out)), "pkv_pool_make_writable")
+        return out.value
+
+    def close(self):
+        if self._h:
+            lib().pkv_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class Trace:

@@ -84,6 +84,10 @@ const DeviceInfo* current_device(int* err) {
   return &info;
 }
 
+unsigned* status_word(int device) {
+  return device >= 0 && device < kMaxDevices ? g_status_addr[device] : nullptr;
+}
+
 static int make_ctx(pkv_stream_t stream, LaunchCtx* ctx) {
   int err = PKV_OK;
   const DeviceInfo* dev = current_device(&err);
@@ -217,6 +221,7 @@ const char* pkv_strerror(int code) {
     case PKV_ERR_DEVICE: return "the current device is not an sm_103 (GB300) GPU";
     case PKV_ERR_STATE: return "trace API misuse";
     case PKV_ERR_SCRATCH: return "batch needs more scratch than PKV_STATIC_SCRATCH_BYTES (use pkv_attend with a workspace)";
+    case PKV_ERR_NOSPACE: return "page pool: not enough free pages";
     default: return "unknown error";
   }
 }

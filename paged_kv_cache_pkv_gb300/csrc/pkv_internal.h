@@ -23,6 +23,9 @@ struct DeviceInfo {
 // Returns nullptr and sets *err when the device is unusable.
 const DeviceInfo* current_device(int* err);
 
+// Device address of the current device's status word.
+unsigned* status_word(int device);
+
 struct LaunchCtx {
   cudaStream_t stream;
   const DeviceInfo* dev;

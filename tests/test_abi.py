@@ -93,7 +93,7 @@ def test_empty_calls_launch_nothing(pkvlib):
 
 
 def test_strerror_covers_every_code(pkvlib):
-    for code in range(0, -10, -1):
+    for code in range(0, -11, -1):
         assert pkvlib.pkv_strerror(code) not in (None, b"unknown error")
     assert pkvlib.pkv_strerror(-99) == b"unknown error"
 
