@@ -8,8 +8,9 @@ pool 1.25x the need, bf16 N(0,1) values from a fixed seed.
 
 Prints ONE JSON line (rank 0).  value = decode tokens/s of the whole job
 (query rows per step x steps / time, max over ranks).  The pool (~0.75 GB) is
-larger than L2 and L2 is also flushed (256 MiB write) before every timed step,
-outside the step's CUDA-event pair.
+larger than L2 and L2 is also flushed before every timed step, outside the
+step's CUDA-event pair: a 256 MiB write, then a 256 MiB read of another buffer
+so that no dirty lines are left for the step to write back.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload IDX]
         python bench.py --impl reference ...   (float64 CPU oracle, same metric)
@@ -210,7 +211,7 @@ def config_of(b, idx):
             "num_q_heads": b.num_q_heads, "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim,
             "page_size": b.page_size, "pool_pages": b.num_blocks,
             "context_tokens": int(b.seq_lens.astype(np.int64).sum()),
-            "l2": "pool larger than L2; 256 MiB L2 flush before every timed step (outside its events)"}
+            "l2": "pool larger than L2; L2 flushed before every timed step, outside its events (256 MiB write, then a 256 MiB read so no dirty lines remain)"}
 
 
 # ---------------------------------------------------------------------------
@@ -236,7 +237,16 @@ def main():
     desc = pkv.make_desc(kc, b.num_q_heads, bt.shape[1])
     ws = torch.empty(pkv.workspace_size(desc, b.B, b.T, dev, int(b.info.get("shared_prefix_pages", 0))),
                      dtype=torch.uint8, device=dev)
+    # L2 flush before every step: write 256 MiB, then read another 256 MiB, so
+    # that L2 holds neither the step's inputs nor dirty lines whose write-back
+    # would otherwise land inside the next step's timed region.
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    evict = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        flush.zero_()
+        evict.sum()
+
     stream = torch.cuda.current_stream(dev)
 
     max_q = int(b.q_lens.max())  # the scheduler knows its largest query chunk
@@ -248,7 +258,7 @@ def main():
                    shared_prefix_pages=prefix)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
     torch.cuda.synchronize()
     if pkv.get_last_error():
@@ -262,7 +272,7 @@ def main():
     torch.cuda.synchronize()
     launches0 = pkv.launch_count()
     for i in range(args.steps):
-        flush.zero_()
+        flush_l2()
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -283,7 +293,7 @@ def main():
     trace = pkv.Trace(capacity=args.steps * 8 + 16)
     with trace:
         for i in range(args.steps):
-            flush.zero_()
+            flush_l2()
             step()
     torch.cuda.synchronize()
 
@@ -334,7 +344,7 @@ def main():
     torch.cuda.synchronize()
     e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
     for i in range(e2e_steps):
-        flush.zero_()
+        flush_l2()
         e_ev[i][0].record(stream)
         e2e_step()
         e_ev[i][1].record(stream)

@@ -56,6 +56,13 @@ __all__ = [
     "attend_one",
     "split_partials",
     "merge_partials",
+    "e4m3_to_f64",
+    "e4m3_encode",
+    "row_scale_exponent",
+    "quantize_rows",
+    "write_fp8",
+    "gather_fp8",
+    "attend_fp8",
 ]
 
 
@@ -158,6 +165,17 @@ def attend(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale,
     query rows are computed (others stay NaN) -- used to sample big batches.
     Returns [T, Hq, D] float64.
     """
+    def fetch(b, L):
+        return (gather(k_cache, block_tables[b], L, page_size),
+                gather(v_cache, block_tables[b], L, page_size))
+    return _attend_batch(q, fetch, seq_lens, query_start_loc, scale, num_q_heads,
+                         num_kv_heads, rows)
+
+
+def _attend_batch(q, fetch, seq_lens, query_start_loc, scale, num_q_heads,
+                  num_kv_heads, rows):
+    """The per-sequence loop of attend; fetch(b, L) returns sequence b's
+    gathered float64 K and V, each [L, Hkv, D]."""
     if num_q_heads % num_kv_heads != 0:
         raise ValueError("num_q_heads must be a multiple of num_kv_heads")
     group = num_q_heads // num_kv_heads
@@ -176,8 +194,7 @@ def attend(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale,
             raise ValueError(f"sequence {b}: {n} queries but only {L} tokens")
         if want is not None and not any(r in want for r in range(q0, q1)):
             continue
-        K = gather(k_cache, block_tables[b], L, page_size)
-        V = gather(v_cache, block_tables[b], L, page_size)
+        K, V = fetch(b, L)
         for j in range(n):
             if want is not None and (q0 + j) not in want:
                 continue
@@ -216,3 +233,137 @@ def merge_partials(parts):
     num = sum(np.exp(m - M) * o for m, _, o in parts)
     den = sum(np.exp(m - M) * l for m, l, _ in parts)
     return num / den
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) pages
+# ---------------------------------------------------------------------------
+# The pages do not describe 8-bit KV pages; this part follows the OCP "8-bit
+# Floating Point Specification (OFP8)", format E4M3: 1 sign bit, 4 exponent
+# bits with bias 7, 3 mantissa bits; exponent field 0 holds the subnormals
+# m * 2^-9; S.1111.111 is NaN; there are no infinities, so the largest finite
+# magnitude is 1.75 * 2^8 = 448.
+#
+# Readings taken here (listed in the design doc):
+#   * one scale per (page, kv head, row): a page fills one token per decode
+#     step, so a single per-page scale would force re-encoding rows already
+#     stored whenever a later token raised the page's maximum; a per-row scale
+#     keeps the write a pure scatter.  The 16 scales of a (page, kv head) are
+#     stored next to its codes.
+#   * the scale is a power of two 2^e, stored as the byte e + 127 (as in the
+#     E8M0 scale type of the OCP microscaling formats), with e the smallest
+#     integer for which max|x| <= 448 * 2^e, clamped to [-126, 127];
+#     x * 2^-e is then exact and the only rounding is the E4M3 one.
+#   * rounding is to nearest, ties to the even code; the sign is kept, so a
+#     negative value that rounds to zero gives the code 0x80 (-0).
+
+E4M3_MAX = 448.0
+
+
+def e4m3_to_f64(codes):
+    """Exact value of E4M3 codes (uint8 array) as float64; 0x7F/0xFF are NaN."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    expo = (c >> 3) & 0xF
+    mant = c & 0x7
+    mag = np.where(expo == 0, mant * 2.0 ** -9, (1.0 + mant / 8.0) * np.exp2(expo - 7.0))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return np.where((c & 0x80) != 0, -mag, mag)
+
+
+_E4M3_POS = None
+
+
+def _e4m3_positive_table():
+    """Values of codes 0x00..0x7E (non-negative, finite), increasing."""
+    global _E4M3_POS
+    if _E4M3_POS is None:
+        _E4M3_POS = e4m3_to_f64(np.arange(0x7F, dtype=np.uint8))
+    return _E4M3_POS
+
+
+def e4m3_encode(x):
+    """Nearest E4M3 code of float64 values with |x| <= 448 (ties to the even
+    code, sign kept).  Raises for non-finite or out-of-range input."""
+    x = np.asarray(x, dtype=np.float64)
+    if not np.all(np.isfinite(x)) or np.any(np.abs(x) > E4M3_MAX):
+        raise ValueError("e4m3_encode takes finite values with |x| <= 448")
+    table = _e4m3_positive_table()
+    a = np.abs(x)
+    lo = np.searchsorted(table, a, side="right") - 1      # largest code value <= a
+    hi = np.minimum(lo + 1, 0x7E)
+    d_lo, d_hi = a - table[lo], table[hi] - a
+    take_hi = (hi != lo) & ((d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0)))
+    code = np.where(take_hi, hi, lo).astype(np.int64)
+    code = code | (np.signbit(x).astype(np.int64) << 7)
+    return code.astype(np.uint8)
+
+
+def row_scale_exponent(amax):
+    """Smallest integer e with amax <= 448 * 2^e, clamped to [-126, 127]."""
+    amax = float(amax)
+    if amax == 0.0:
+        return -126
+    e = int(np.floor(np.log2(amax / E4M3_MAX)))
+    while amax > E4M3_MAX * 2.0 ** e:
+        e += 1
+    while amax <= E4M3_MAX * 2.0 ** (e - 1):
+        e -= 1
+    return min(max(e, -126), 127)
+
+
+def quantize_rows(x_bits):
+    """E4M3 codes and scale bytes of bf16 rows.
+
+    ``x_bits`` [..., D] uint16 (bf16 bits).  Each row (last axis) gets
+    e = row_scale_exponent(max |x|); its codes are e4m3_encode(x * 2^-e) and
+    its scale byte is e + 127.  Returns (codes [..., D] uint8, scale [...] uint8).
+    """
+    x = bf16_to_f64(x_bits)
+    amax = np.abs(x).max(axis=-1)
+    e = np.vectorize(row_scale_exponent, otypes=[np.int64])(amax)
+    codes = e4m3_encode(x * np.exp2(-e.astype(np.float64))[..., None])
+    return codes, (e + 127).astype(np.uint8)
+
+
+def write_fp8(k_new, v_new, slot_mapping, k_codes, v_codes, k_scale, v_scale, page_size):
+    """KV write into FP8 pages: each new (token, kv head) row of K and of V is
+    quantised with quantize_rows and scattered like ``write``; its scale byte
+    goes to [page, head, row] of k_scale / v_scale.
+
+    Shapes: k_new/v_new [T, Hkv, D] uint16; codes [NB, Hkv, P, D] uint8;
+    scales [NB, Hkv, P] uint8.  Returns new (k_codes, v_codes, k_scale, v_scale).
+    """
+    kc, vc = np.array(k_codes, copy=True), np.array(v_codes, copy=True)
+    ks, vs = np.array(k_scale, copy=True), np.array(v_scale, copy=True)
+    kq, kqs = quantize_rows(np.asarray(k_new))
+    vq, vqs = quantize_rows(np.asarray(v_new))
+    for t, s in enumerate(np.asarray(slot_mapping, dtype=np.int64)):
+        if s < 0:
+            continue
+        page, row = divmod(int(s), int(page_size))
+        if page >= kc.shape[0]:
+            raise IndexError(f"slot {int(s)} of token {t} is outside the pool")
+        kc[page, :, row, :], ks[page, :, row] = kq[t], kqs[t]
+        vc[page, :, row, :], vs[page, :, row] = vq[t], vqs[t]
+    return kc, vc, ks, vs
+
+
+def gather_fp8(codes, scales, block_table_row, seq_len, page_size):
+    """Contiguous float64 values of one sequence's FP8 rows: code value times
+    2^(scale byte - 127).  Returns [seq_len, Hkv, D]."""
+    j = np.arange(int(seq_len))
+    pages = np.asarray(block_table_row)[j // page_size]
+    rows = j % page_size
+    val = e4m3_to_f64(codes[pages, :, rows, :])
+    return val * np.exp2(scales[pages, :, rows].astype(np.float64) - 127.0)[..., None]
+
+
+def attend_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, seq_lens,
+               query_start_loc, scale, num_q_heads, num_kv_heads, page_size, rows=None):
+    """attend() over FP8 pages: the same textbook attention, with K and V the
+    exact values the codes and scales stand for."""
+    def fetch(b, L):
+        return (gather_fp8(k_codes, k_scale, block_tables[b], L, page_size),
+                gather_fp8(v_codes, v_scale, block_tables[b], L, page_size))
+    return _attend_batch(q, fetch, seq_lens, query_start_loc, scale, num_q_heads,
+                         num_kv_heads, rows)

@@ -299,9 +299,10 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
     for (int s = 0; s < kDecStages; ++s) mbar_init(&R.bar[s], 1);
     fence_mbar_init();
   }
-  // Everything above overlaps the previous kernel under programmatic
-  // dependent launch; inputs are read only after this point.
-  griddep_wait();
+  // Under programmatic dependent launch everything up to griddep_wait() below
+  // (plan, cursor, first block ids) overlaps the previous kernel.  It reads
+  // only seq_lens, query_start_loc and block_tables, which pkv_write never
+  // writes; the pools are read only after the wait.
 
   // ---- plan: per-sequence unit counts and their exclusive prefix ----------
   const int per_row = p.Hkv * p.nsub;
@@ -396,6 +397,7 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
       bulk_g2s(&R.kv[stage][1][0], p.v_cache + off, kPageBytes, &R.bar[stage], policy);
     }
   };
+  griddep_wait();
   {
     const int prologue = min(kDecStages, n_units);
     for (int s = 0; s < prologue; ++s) {
