@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
+                    help="page format: bf16, or E4M3 codes with per-row scale bytes")
     return ap.parse_args()
 
 
@@ -156,20 +158,29 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # the oracle as CPU baseline / reference arm
 # ---------------------------------------------------------------------------
-def oracle_sample(batch, max_rows, min_seconds=0.0, max_reps=50):
+def oracle_sample(batch, max_rows, min_seconds=0.0, max_reps=50, fp8_pools=None):
     """Time the float64 oracle (write + attend) on the first ``max_rows`` query
-    rows of the batch, single-threaded; returns (tokens/s, rows, seconds)."""
+    rows of the batch, single-threaded; returns (tokens/s, rows, seconds).
+    ``fp8_pools`` (codes and scales) selects the FP8-page oracle."""
     import oracle.pkv_oracle as O
     b16 = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
     q, kn, vn = b16(batch.q), b16(batch.k_new), b16(batch.v_new)
-    kc, vc = b16(batch.k_cache), b16(batch.v_cache)
+    if fp8_pools is None:
+        kc, vc = b16(batch.k_cache), b16(batch.v_cache)
+    else:
+        pools8 = [t.contiguous().cpu().numpy() for t in fp8_pools]
     rows = list(range(min(max_rows, batch.T)))
+    args = (batch.block_tables, batch.seq_lens, batch.query_start_loc, batch.scale,
+            batch.num_q_heads, batch.num_kv_heads, batch.page_size)
     total, reps, t0 = 0.0, 0, time.perf_counter()
     while True:
         s = time.perf_counter()
-        k2, v2 = O.write(kn, vn, batch.slot_mapping, kc, vc, batch.page_size)
-        O.attend(q, k2, v2, batch.block_tables, batch.seq_lens, batch.query_start_loc, batch.scale,
-                 batch.num_q_heads, batch.num_kv_heads, batch.page_size, rows=rows)
+        if fp8_pools is None:
+            k2, v2 = O.write(kn, vn, batch.slot_mapping, kc, vc, batch.page_size)
+            O.attend(q, k2, v2, *args, rows=rows)
+        else:
+            w = O.write_fp8(kn, vn, batch.slot_mapping, *pools8, batch.page_size)
+            O.attend_fp8(q, *w, *args, rows=rows)
         total += time.perf_counter() - s
         reps += 1
         if time.perf_counter() - t0 >= min_seconds or reps >= max_reps:
@@ -180,15 +191,16 @@ def oracle_sample(batch, max_rows, min_seconds=0.0, max_reps=50):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    from workloads import workload
+    from workloads import fp8_pools, workload
     b = workload(args.workload, device="cpu")
+    pools8 = fp8_pools(b, b.info["seed"] + 1) if args.kv == "fp8" else None
     steps, warm = args.steps, args.warmup
     # each step: the oracle over a bounded sample (4 rows) of the workload
     rows = 4
     times = []
     for i in range(warm + steps):
         s = time.perf_counter()
-        rate, n, _ = oracle_sample(b, rows, max_reps=1)
+        rate, n, _ = oracle_sample(b, rows, max_reps=1, fp8_pools=pools8)
         if i >= warm:
             times.append(time.perf_counter() - s)
         if i >= warm and sum(times) > 120:
@@ -198,16 +210,18 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": done, "warmup": warm, "ms_per_step": 1e3 * sum(times) / done,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_of(b, args.workload),
+            "data": "synthetic", "config": config_of(b, args.workload, args.kv),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                              "sample": f"{rows} query rows (with the full write) of the workload per step"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def config_of(b, idx):
+def config_of(b, idx, kv="bf16"):
     from workloads import WORKLOADS
-    return {"workload": f"cfg{idx}: {WORKLOADS[idx]}", "num_seqs": b.B, "query_rows": b.T,
+    return {"workload": f"cfg{idx}: {WORKLOADS[idx]}" + (", FP8 (E4M3) pages" if kv == "fp8" else ""),
+            "kv_pages": "bf16" if kv == "bf16" else "E4M3 codes + one power-of-two scale byte per row",
+            "num_seqs": b.B, "query_rows": b.T,
             "num_q_heads": b.num_q_heads, "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim,
             "page_size": b.page_size, "pool_pages": b.num_blocks,
             "context_tokens": int(b.seq_lens.astype(np.int64).sum()),
@@ -224,7 +238,7 @@ def main():
         run_reference(args, rank, world)
         return
     import paged_kv_cache_pkv_gb300 as pkv
-    from workloads import kv_bytes, workload
+    from workloads import fp8_pools, kv_bytes, workload
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -232,7 +246,12 @@ def main():
     t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).to(dev)
     slots, bt, lens, qsl = (t(b.slot_mapping, np.int64), t(b.block_tables, np.int32),
                             t(b.seq_lens, np.int32), t(b.query_start_loc, np.int32))
-    kc, vc = b.k_cache, b.v_cache
+    fp8 = args.kv == "fp8"
+    if fp8:
+        kc, vc, ks, vs = fp8_pools(b, b.info["seed"] + 1)
+        b.k_cache = b.v_cache = None  # the bf16 pool is not used
+    else:
+        kc, vc = b.k_cache, b.v_cache
     out = torch.empty_like(b.q)
     desc = pkv.make_desc(kc, b.num_q_heads, bt.shape[1])
     ws = torch.empty(pkv.workspace_size(desc, b.B, b.T, dev, int(b.info.get("shared_prefix_pages", 0))),
@@ -252,7 +271,14 @@ def main():
     max_q = int(b.q_lens.max())  # the scheduler knows its largest query chunk
     prefix = int(b.info.get("shared_prefix_pages", 0))  # and the prefix its sequences share
 
+    if fp8 and prefix:
+        raise SystemExit("FP8 pages have no shared-prefix cascade; pick another workload")
+
     def step():
+        if fp8:
+            pkv.write_fp8(b.k_new, b.v_new, slots, kc, vc, ks, vs)
+            pkv.attend_fp8(b.q, kc, vc, ks, vs, bt, lens, qsl, b.scale, out=out, workspace=ws)
+            return
         pkv.write(b.k_new, b.v_new, slots, kc, vc)
         pkv.attend(b.q, kc, vc, bt, lens, qsl, b.scale, out=out, workspace=ws, max_query_len=max_q,
                    shared_prefix_pages=prefix)
@@ -297,7 +323,7 @@ def main():
             step()
     torch.cuda.synchronize()
 
-    uniq = kv_bytes(b, unique=True)
+    uniq = kv_bytes(b, unique=True, fp8=fp8)
     qo_bytes = 2 * b.q.numel() * 2
     meta_bytes = 4 * (b.block_tables.size + 2 * b.B + 1)
     alg_bytes = uniq + qo_bytes + meta_bytes
@@ -311,7 +337,8 @@ def main():
     try:
         with open(TRAFFIC_FILE) as f:
             tr = dict(l.split(": ", 1) for l in f.read().splitlines() if ": " in l and " " not in l.split(": ")[0])
-        if tr.get("kernel_hash") == kernel_hash() and int(tr.get("workload", -1)) == args.workload:
+        if tr.get("kernel_hash") == kernel_hash() and int(tr.get("workload", -1)) == args.workload \
+                and not fp8:
             traffic = int(tr["dram_bytes_per_launch"])
     except (OSError, ValueError, KeyError):
         pass
@@ -334,9 +361,14 @@ def main():
     def e2e_step():
         for name, x in host.items():
             dev_in[name].copy_(x, non_blocking=True)
-        pkv.write(dev_in["k_new"], dev_in["v_new"], dev_in["slots"], kc, vc)
-        pkv.attend(dev_in["q"], kc, vc, dev_in["bt"], dev_in["lens"], dev_in["qsl"], b.scale, out=out,
-                   workspace=ws, max_query_len=max_q, shared_prefix_pages=prefix)
+        if fp8:
+            pkv.write_fp8(dev_in["k_new"], dev_in["v_new"], dev_in["slots"], kc, vc, ks, vs)
+            pkv.attend_fp8(dev_in["q"], kc, vc, ks, vs, dev_in["bt"], dev_in["lens"], dev_in["qsl"],
+                           b.scale, out=out, workspace=ws)
+        else:
+            pkv.write(dev_in["k_new"], dev_in["v_new"], dev_in["slots"], kc, vc)
+            pkv.attend(dev_in["q"], kc, vc, dev_in["bt"], dev_in["lens"], dev_in["qsl"], b.scale, out=out,
+                       workspace=ws, max_query_len=max_q, shared_prefix_pages=prefix)
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -354,7 +386,8 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, rows, secs = oracle_sample(b, b.T, min_seconds=10.0)
+        rate, rows, secs = oracle_sample(b, b.T, min_seconds=10.0,
+                                         fp8_pools=(kc, vc, ks, vs) if fp8 else None)
         cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"all {rows} query rows of one step (write + attend), repeated for {secs:.1f} s, "
                          "single-threaded NumPy float64"}
@@ -364,9 +397,9 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": config_of(b, args.workload),
-            "hbm": {"unique_kv_bytes": uniq, "logical_kv_bytes": kv_bytes(b, unique=False),
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+            "data": "synthetic", "config": config_of(b, args.workload, args.kv),
+            "hbm": {"unique_kv_bytes": uniq, "logical_kv_bytes": kv_bytes(b, unique=False, fp8=fp8),
                     "step_gbs": alg_bytes / (total_s / args.steps / world) / 1e9,
                     "step_frac_of_8tbs": alg_bytes / (total_s / args.steps / world) / 1e9 / NOMINAL_HBM_GBS,
                     "decode_kernel_frac_of_8tbs": achieved / NOMINAL_HBM_GBS},

@@ -60,6 +60,7 @@ extern "C" {
 #endif
 
 typedef uint16_t pkv_bf16;                 /* raw bfloat16 bits             */
+typedef uint8_t pkv_fp8;                   /* E4M3 code (see FP8 pages)     */
 typedef struct CUstream_st* pkv_stream_t;  /* same handle as cudaStream_t   */
 typedef struct CUevent_st* pkv_event_t;    /* same handle as cudaEvent_t    */
 
@@ -207,6 +208,47 @@ PKV_API int pkv_attend_static(const pkv_bf16* q, const pkv_bf16* k_cache,
                               int32_t max_query_len, int32_t shared_prefix_pages,
                               float scale, pkv_bf16* out, const pkv_desc* desc,
                               pkv_stream_t stream);
+
+/* ---- FP8 pages ------------------------------------------------------------ */
+/* KV pages of 8-bit E4M3 codes (OCP 8-bit Floating Point Specification: sign,
+ * 4 exponent bits with bias 7, 3 mantissa bits; largest magnitude 448) with
+ * one power-of-two scale per row, halving the bytes decode reads.  The pages
+ * this library follows do not describe 8-bit pages; the format is the OCP one
+ * and the scaling is this library's:
+ *   k_cache, v_cache  [num_blocks, num_kv_heads, 16, 128] E4M3 codes (2 KiB
+ *                     per page and head); k_scale, v_scale [num_blocks,
+ *                     num_kv_heads, 16] bytes: row (page, head, r) holds the
+ *                     values code * 2^(scale - 127).
+ * A single scale per page would have to be fixed before the page's later
+ * tokens are known (a page fills one token per decode step), so each row of
+ * a page carries its own.  All four arrays 16-byte aligned, device. */
+
+/* pkv_write_fp8 -- pkv_write into FP8 pages.  Each new (token, kv head) row
+ * of K and of V (bf16) gets e = the smallest integer with max|x| <= 448 * 2^e,
+ * clamped to [-126, 127]; its codes are x * 2^-e rounded to the nearest E4M3
+ * value (ties to even, sign kept, so -0 and negative values that round to 0
+ * give 0x80) and its scale byte is e + 127.  Inputs must be finite.  Slots,
+ * skipping and PKV_STATUS_BAD_SLOT as in pkv_write.  Deterministic: the same
+ * row always gives the same bytes. */
+PKV_API int pkv_write_fp8(const pkv_bf16* k_new, const pkv_bf16* v_new,
+                          const int64_t* slot_mapping, int64_t num_tokens,
+                          pkv_fp8* k_cache, pkv_fp8* v_cache, uint8_t* k_scale,
+                          uint8_t* v_scale, const pkv_desc* desc, pkv_stream_t stream);
+
+/* pkv_attend_fp8 -- pkv_attend over FP8 pages: the same result with K and V
+ * the exact values code * 2^(scale - 127).  Every query row runs on the
+ * split-KV kernel (no tensor-core prefill and no shared-prefix cascade for
+ * FP8 pages).  workspace: at least pkv_attend_workspace_size(desc, num_seqs,
+ * num_tokens, 0) bytes.  Scale bytes of rows a query sees must lie in
+ * [1, 254] (pkv_write_fp8 writes nothing else); rows it does not see are
+ * never used, whatever they hold. */
+PKV_API int pkv_attend_fp8(const pkv_bf16* q, const pkv_fp8* k_cache,
+                           const pkv_fp8* v_cache, const uint8_t* k_scale,
+                           const uint8_t* v_scale, const int32_t* block_tables,
+                           const int32_t* seq_lens, const int32_t* query_start_loc,
+                           int32_t num_seqs, int32_t num_tokens, float scale,
+                           pkv_bf16* out, void* workspace, size_t workspace_bytes,
+                           const pkv_desc* desc, pkv_stream_t stream);
 
 /* ---- page pool (host side) ------------------------------------------------ */
 /* The engine reserves num_gpu_blocks pages of block_size tokens (vLLM notes

@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "PkvError", "PkvUnavailable", "lib", "library_path", "Desc", "write", "attend",
     "workspace_size", "get_last_error", "launch_count", "Trace", "PagePool", "KERNELS",
-    "export_pages", "import_pages",
+    "export_pages", "import_pages", "write_fp8", "attend_fp8",
     "STATUS_BAD_SLOT", "STATUS_BAD_BLOCK", "STATUS_BAD_QUERY", "STATUS_TIMEOUT",
 ]
 
@@ -56,6 +56,9 @@ _SIGS = {
                                   _vp, _vp, _sz, ctypes.POINTER(Desc), _vp]),
     "pkv_attend_static": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                          ctypes.c_float, _vp, ctypes.POINTER(Desc), _vp]),
+    "pkv_write_fp8": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, ctypes.POINTER(Desc), _vp]),
+    "pkv_attend_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float,
+                                      _vp, _vp, _sz, ctypes.POINTER(Desc), _vp]),
     "pkv_get_last_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
     "pkv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_launch_count": (ctypes.c_uint64, []),
@@ -199,6 +202,74 @@ def attend(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, 
                                 _ptr(workspace), workspace.numel(), ctypes.byref(desc),
                                 _stream(q.device, stream)),
                "pkv_attend")
+    return out
+
+
+def _need_fp8_pool(k_cache, v_cache, k_scale, v_scale):
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.uint8, 4)
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need(t, n, torch.uint8, 3)
+    if k_cache.shape != v_cache.shape or k_scale.shape != v_scale.shape or \
+            tuple(k_scale.shape) != tuple(k_cache.shape[:3]):
+        raise ValueError("FP8 pools must be codes [NB, Hkv, P, D] and scales [NB, Hkv, P]")
+
+
+def write_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, stream=None):
+    """pkv_write into FP8 pages: new bf16 rows [T, Hkv, D] are encoded as E4M3
+    codes (uint8 pools [NB, Hkv, P, D]) with one power-of-two scale byte per
+    row (uint8 [NB, Hkv, P]).  In place, stream-ordered."""
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need_fp8_pool(k_cache, v_cache, k_scale, v_scale)
+    T = k_new.shape[0]
+    if k_new.shape != v_new.shape or slot_mapping.shape[0] != T or \
+            k_new.shape[1:] != (k_cache.shape[1], k_cache.shape[3]):
+        raise ValueError("k_new must be [T, Hkv, D] matching the pool and slot_mapping")
+    desc = make_desc(k_cache, k_cache.shape[1], 1)
+    with torch.cuda.device(k_cache.device):
+        _check(lib().pkv_write_fp8(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), T, _ptr(k_cache),
+                                   _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), ctypes.byref(desc),
+                                   _stream(k_cache.device, stream)),
+               "pkv_write_fp8")
+
+
+def attend_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, query_start_loc, scale,
+               out=None, workspace=None, stream=None):
+    """attend() over FP8 pages (codes and per-row scale bytes as written by
+    write_fp8); every query row runs on the split-KV kernel."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need_fp8_pool(k_cache, v_cache, k_scale, v_scale)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(query_start_loc, "query_start_loc", torch.int32, 1)
+    T, Hq, D = q.shape
+    B = seq_lens.shape[0]
+    if query_start_loc.shape[0] != B + 1 or block_tables.shape[0] != B:
+        raise ValueError("seq_lens [B], query_start_loc [B+1] and block_tables [B, M] disagree")
+    if k_cache.shape[3] != D:
+        raise ValueError("k_cache/q shapes disagree")
+    desc = make_desc(k_cache, Hq, block_tables.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.bfloat16, 3)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    need = workspace_size(desc, B, T, q.device, 0)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    else:
+        _need(workspace, "workspace", torch.uint8)
+        if workspace.numel() < need:
+            raise ValueError(f"workspace needs {need} bytes, got {workspace.numel()}")
+    with torch.cuda.device(q.device):
+        _check(lib().pkv_attend_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                    _ptr(block_tables), _ptr(seq_lens), _ptr(query_start_loc), B, T,
+                                    float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                                    ctypes.byref(desc), _stream(q.device, stream)),
+               "pkv_attend_fp8")
     return out
 
 

@@ -7,6 +7,7 @@
 // writer; unsupported options are rejected up front) and the tensor-lifetime
 // rule of the vLLM notes "EngineCoreClient ..." ("Flujo de datos": buffers
 // stay alive until the asynchronous consumer is done with them).
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
@@ -72,8 +73,13 @@ const DeviceInfo* current_device(int* err) {
   fresh.smem_optin = prop.sharedMemPerBlockOptin;
   // A variant that cannot be resident gets 0 warps; pkv_attend then rejects
   // the head ratios that need it instead of failing here.
-  for (int v = 0; v < 3; ++v)
-    fresh.dec_warps[v] = fresh.sm_count * decode_ctas_per_sm(v) * kDecWarps;
+  for (int v = 0; v < 3; ++v) {
+    fresh.dec_warps[v] = fresh.sm_count * decode_ctas_per_sm(v, false) * kDecWarps;
+    // the FP8 variant shares the bf16 workspace layout, so it never runs on
+    // more warps than the bf16 one
+    fresh.dec_warps_f8[v] =
+        std::min(fresh.dec_warps[v], fresh.sm_count * decode_ctas_per_sm(v, true) * kDecWarps);
+  }
   void* addr = nullptr;
   if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) {
     *err = PKV_ERR_LAUNCH;
@@ -192,6 +198,48 @@ int pkv_attend(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cac
   AttendArgs a{q,          k_cache,    v_cache,    block_tables,  seq_lens,
                query_start_loc, num_seqs, num_tokens, max_query_len, shared_prefix_pages,
                scale,      out,        workspace,  workspace_bytes, *desc};
+  return launch_attend(ctx, a);
+}
+
+int pkv_write_fp8(const pkv_bf16* k_new, const pkv_bf16* v_new, const int64_t* slot_mapping,
+                  int64_t num_tokens, pkv_fp8* k_cache, pkv_fp8* v_cache, uint8_t* k_scale,
+                  uint8_t* v_scale, const pkv_desc* desc, pkv_stream_t stream) {
+  if (int e = check_desc(desc)) return e;
+  if (num_tokens < 0) return PKV_ERR_RANGE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+    return PKV_ERR_NULL;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(slot_mapping, 8))
+    return PKV_ERR_ALIGN;
+  LaunchCtx ctx;
+  if (int e = make_ctx(stream, &ctx)) return e;
+  return launch_write_fp8(ctx, k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, k_scale,
+                          v_scale, desc->num_blocks, desc->num_kv_heads);
+}
+
+int pkv_attend_fp8(const pkv_bf16* q, const pkv_fp8* k_cache, const pkv_fp8* v_cache,
+                   const uint8_t* k_scale, const uint8_t* v_scale, const int32_t* block_tables,
+                   const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_seqs,
+                   int32_t num_tokens, float scale, pkv_bf16* out, void* workspace,
+                   size_t workspace_bytes, const pkv_desc* desc, pkv_stream_t stream) {
+  if (int e = check_desc(desc)) return e;
+  if (num_seqs < 0 || num_tokens < 0) return PKV_ERR_RANGE;
+  if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !k_scale || !v_scale || !block_tables || !seq_lens ||
+      !query_start_loc || !out || !workspace)
+    return PKV_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_scale, 16) ||
+      !aligned(v_scale, 16) || !aligned(out, 16) || !aligned(block_tables, 4) ||
+      !aligned(seq_lens, 4) || !aligned(query_start_loc, 4) || !aligned(workspace, 256))
+    return PKV_ERR_ALIGN;
+  LaunchCtx ctx;
+  if (int e = make_ctx(stream, &ctx)) return e;
+  AttendArgs a{q,     k_cache, v_cache,   block_tables,    seq_lens, query_start_loc,
+               num_seqs, num_tokens, 0, 0, scale, out, workspace, workspace_bytes, *desc};
+  a.fp8 = true;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   return launch_attend(ctx, a);
 }
 

@@ -14,6 +14,8 @@ namespace pkv {
 constexpr int kHeadDim = 128;   // D
 constexpr int kPage = 16;       // tokens per page
 constexpr int kPageBytes = kPage * kHeadDim * 2;  // one (page, kv head): 4 KiB
+constexpr int kPageBytesF8 = kPage * kHeadDim;    // the same in E4M3 codes: 2 KiB
+constexpr int kScaleBytes = kPage;                // FP8 row scales of one (page, kv head)
 
 // Split-KV decode kernel shape.
 #ifndef PKV_DEC_WARPS

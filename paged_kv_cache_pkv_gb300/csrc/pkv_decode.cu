@@ -32,6 +32,13 @@
 //  * PV: lane (dc = lane%16, parity = lane/16) owns dims 8dc..8dc+7 of
 //    even/odd tokens, packed fp32x2 FMAs; probabilities are broadcast through
 //    shared memory as (p, p) pairs.
+//  * FP8 pages (template flag F8): the unit moves a 2 KiB K page and a 2 KiB V
+//    page of E4M3 codes plus their 16-byte blocks of per-row scale bytes
+//    (scale = 2^(byte-127)).  Codes are widened exactly (e4m3 -> f16 -> f32);
+//    the K row scale multiplies the finished score, the V row scale the
+//    probability that weights the row, so no per-element scaling is needed.
+//    A lane then reads 16 consecutive codes of a K row (dims 16c..16c+15) and
+//    8 of a V row, which keeps the shared-memory reads conflict free.
 //  * A warp that sees a whole (row, head group) writes bf16 output directly.
 //    A split one writes (m, l, o) to one of its two partial slots and bumps
 //    an epoch-tagged arrival counter; the last warp to arrive merges the
@@ -43,6 +50,9 @@
 #include <cmath>
 #include <type_traits>
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
 
@@ -50,8 +60,10 @@ namespace pkv {
 
 struct DecodeParams {
   const uint16_t* q;
-  const uint16_t* k_cache;
-  const uint16_t* v_cache;
+  const uint8_t* k_cache;  // bf16 pages, or E4M3 codes for the FP8 variant
+  const uint8_t* v_cache;
+  const uint8_t* k_scale;  // FP8 only: [NB][Hkv][16] scale bytes
+  const uint8_t* v_scale;
   const int32_t* block_tables;
   const int32_t* seq_lens;
   const int32_t* qsl;
@@ -72,13 +84,28 @@ struct StageDesc {
   int32_t row, item, item_start, nvis;
 };
 
+// Bytes of one (page, kv head) of K (or V) in the pool.
+template <bool F8>
+constexpr int kPageBytesOf = F8 ? kPageBytesF8 : kPageBytes;
+
 // One warp's page ring.
+template <bool F8>
 struct __align__(128) DecRing {
-  uint4 kv[kDecStages][2][kPageBytes / 16];  // [stage][K|V][16 rows x 16 vec]
-  float2 ps[kPage * kMaxGroupPerItem];        // (p, p) pairs [token][head]
+  uint4 kv[kDecStages][2][kPageBytesOf<F8> / 16];  // [stage][K|V][16 rows]
+  uint4 sc[kDecStages][F8 ? 2 : 1];                // FP8: K and V row scales
+  float2 ps[kPage * kMaxGroupPerItem];              // (p, p) pairs [token][head]
   StageDesc desc[kDecStages];
   uint64_t bar[kDecStages];
 };
+
+// Exact widening of two E4M3 codes (low byte first) to floats.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
+  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+  return __half22float2(*reinterpret_cast<const __half2*>(&r));
+}
+
+// 2^(byte - 127) for a scale byte in [1, 254].
+__device__ __forceinline__ float scale_of(uint32_t byte) { return __uint_as_float(byte << 23); }
 
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr float kTau = 8.0f;  // log2-domain slack before the running max moves
@@ -283,13 +310,14 @@ __device__ __forceinline__ void merge_item(const DecodeParams& p, int lane, int 
   }
 }
 
-template <int GH>
+template <int GH, bool F8>
 __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
-  DecRing& R = reinterpret_cast<DecRing*>(smem_raw)[wib];
-  int* s_start = reinterpret_cast<int*>(smem_raw + sizeof(DecRing) * kDecWarps);
+  using Ring = DecRing<F8>;
+  Ring& R = reinterpret_cast<Ring*>(smem_raw)[wib];
+  int* s_start = reinterpret_cast<int*>(smem_raw + sizeof(Ring) * kDecWarps);
   int* s_q0 = s_start + (p.B + 1);
   int* s_len = s_q0 + (p.B + 1);
   const SeqSmem sq{s_start, s_q0, s_len};
@@ -389,12 +417,17 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
   }
   auto issue = [&](int stage) {
     if (lane == 0) {
+      constexpr int PB = kPageBytesOf<F8>;
       const int g = pc.item / p.nsub;
-      const size_t off = (size_t(pc.bid) * p.Hkv + g) * (kPageBytes / 2);
+      const size_t ph = size_t(pc.bid) * p.Hkv + g;  // (page, kv head)
       R.desc[stage] = StageDesc{pc.q0 + pc.j, pc.item, pc.item_start, pc.nvis - p.np * kPage};
-      mbar_arrive_expect_tx(&R.bar[stage], 2 * kPageBytes);
-      bulk_g2s(&R.kv[stage][0][0], p.k_cache + off, kPageBytes, &R.bar[stage], policy);
-      bulk_g2s(&R.kv[stage][1][0], p.v_cache + off, kPageBytes, &R.bar[stage], policy);
+      mbar_arrive_expect_tx(&R.bar[stage], 2 * PB + (F8 ? 2 * kScaleBytes : 0));
+      bulk_g2s(&R.kv[stage][0][0], p.k_cache + ph * PB, PB, &R.bar[stage], policy);
+      bulk_g2s(&R.kv[stage][1][0], p.v_cache + ph * PB, PB, &R.bar[stage], policy);
+      if constexpr (F8) {
+        bulk_g2s(&R.sc[stage][0], p.k_scale + ph * kScaleBytes, kScaleBytes, &R.bar[stage], policy);
+        bulk_g2s(&R.sc[stage][1], p.v_scale + ph * kScaleBytes, kScaleBytes, &R.bar[stage], policy);
+      }
     }
   };
   griddep_wait();
@@ -431,8 +464,9 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
     const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (size_t(d.row) * p.Hq + cur_h0) * kHeadDim);
 #pragma unroll
     for (int h = 0; h < GH; ++h) {
-      const uint4 a = __ldg(qrow + h * 16 + c8);
-      const uint4 b = __ldg(qrow + h * 16 + 8 + c8);
+      // the lane's dims: {8c..8c+7, 64+8c..64+8c+7} (bf16), 16c..16c+15 (FP8)
+      const uint4 a = __ldg(qrow + h * 16 + (F8 ? 2 * c8 : c8));
+      const uint4 b = __ldg(qrow + h * 16 + (F8 ? 2 * c8 + 1 : 8 + c8));
       const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -629,21 +663,41 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
     const uint4* Vs = R.kv[stage][1];
 
     // ---- V slice of this lane into registers (even/odd tokens x 8 dims) ----
-    uint4 vreg[kPage / 2];
+    using VVec = std::conditional_t<F8, uint2, uint4>;  // 8 dims of one row
+    VVec vreg[kPage / 2];
 #pragma unroll
-    for (int i = 0; i < kPage / 2; ++i) vreg[i] = Vs[(par + 2 * i) * 16 + dc];
+    for (int i = 0; i < kPage / 2; ++i)
+      vreg[i] = reinterpret_cast<const VVec*>(Vs)[(par + 2 * i) * 16 + dc];
+    // FP8: the row scales of this lane's score token, read before the stage
+    // goes back to the copy engine
+    float kscale = 1.f, vscale = 1.f;
+    if constexpr (F8) {
+      const uint8_t* sc = reinterpret_cast<const uint8_t*>(&R.sc[stage][0]);
+      kscale = scale_of(sc[my_tok]);
+      vscale = scale_of(sc[kScaleBytes + my_tok]);
+    }
 
     // ---- scores: 4 tokens x GH heads per lane, partial over 16 dims ----
     float v[4 * GH];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int t = grp + 4 * i;
-      const uint4 a = Ks[t * 16 + c8];
-      const uint4 b = Ks[t * 16 + 8 + c8];
-      const uint32_t wk[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
       float2 kf[8];
+      if constexpr (F8) {
+        const uint4 a = Ks[t * 8 + c8];  // codes of dims 16c..16c+15
+        const uint32_t wk[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) kf[e] = make_float2(bf_lo(wk[e]), bf_hi(wk[e]));
+        for (int e = 0; e < 4; ++e) {
+          kf[2 * e] = e4m3x2_to_float2(wk[e] & 0xFFFFu);
+          kf[2 * e + 1] = e4m3x2_to_float2(wk[e] >> 16);
+        }
+      } else {
+        const uint4 a = Ks[t * 16 + c8];
+        const uint4 b = Ks[t * 16 + 8 + c8];
+        const uint32_t wk[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) kf[e] = make_float2(bf_lo(wk[e]), bf_hi(wk[e]));
+      }
 #pragma unroll
       for (int h = 0; h < GH; ++h) {
         float2 acc = __fmul2_rn(qf[h][0], kf[0]);
@@ -689,7 +743,7 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
     }
     float s[NVL];
 #pragma unroll
-    for (int k = 0; k < NVL; ++k) s[k] = my_tok < nvalid ? v[k] : -INFINITY;
+    for (int k = 0; k < NVL; ++k) s[k] = my_tok < nvalid ? v[k] * kscale : -INFINITY;
 
     // ---- online softmax (log2 domain) ----
     float mine[NVL];
@@ -757,6 +811,8 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
     for (int k = 0; k < NVL; ++k) {
       pr[k] = ex2(s[k] - mine[k]);
       lsum[k] += pr[k];
+      // FP8: weight the row's codes by p * 2^(V scale) (masked rows stay 0)
+      if constexpr (F8) pr[k] = my_tok < nvalid ? pr[k] * vscale : 0.f;
     }
     if constexpr (GH == 4) {
       *reinterpret_cast<float4*>(&R.ps[my_tok * 4 + 2 * h3]) = make_float4(pr[0], pr[0], pr[1], pr[1]);
@@ -772,10 +828,19 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
     for (int i = 0; i < kPage / 2; ++i) {
       const int t = par + 2 * i;
       if (nvalid == kPage || t < nvalid) {
-        const uint32_t wv[4] = {vreg[i].x, vreg[i].y, vreg[i].z, vreg[i].w};
         float2 vf[4];
+        if constexpr (F8) {
+          const uint32_t wv[2] = {vreg[i].x, vreg[i].y};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) vf[e] = make_float2(bf_lo(wv[e]), bf_hi(wv[e]));
+          for (int e = 0; e < 2; ++e) {
+            vf[2 * e] = e4m3x2_to_float2(wv[e] & 0xFFFFu);
+            vf[2 * e + 1] = e4m3x2_to_float2(wv[e] >> 16);
+          }
+        } else {
+          const uint32_t wv[4] = {vreg[i].x, vreg[i].y, vreg[i].z, vreg[i].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) vf[e] = make_float2(bf_lo(wv[e]), bf_hi(wv[e]));
+        }
         float2 pv[GH];
         if constexpr (GH == 4) {
           const float4 x = *reinterpret_cast<const float4*>(&R.ps[t * 4]);
@@ -817,14 +882,15 @@ static int variant_of(int gh) { return gh == 4 ? 2 : gh - 1; }
 
 // Rings, then the plan's per-sequence arrays: unit prefix and query_start_loc
 // ([B+1] each) and seq_lens ([B]).
+template <bool F8>
 static size_t decode_smem_bytes(int num_seqs) {
-  return sizeof(DecRing) * kDecWarps + sizeof(int) * (3 * size_t(num_seqs) + 2);
+  return sizeof(DecRing<F8>) * kDecWarps + sizeof(int) * (3 * size_t(num_seqs) + 2);
 }
 
-template <int GH>
+template <int GH, bool F8>
 static int occupancy_for() {
-  auto fn = pkv_decode_kernel<GH>;
-  const size_t smem = decode_smem_bytes(kMaxSeqs);
+  auto fn = pkv_decode_kernel<GH, F8>;
+  const size_t smem = decode_smem_bytes<F8>(kMaxSeqs);
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess) {
     cudaGetLastError();  // not sticky; leave no error behind for later launches
     return 0;
@@ -837,11 +903,11 @@ static int occupancy_for() {
   return blocks;
 }
 
-int decode_ctas_per_sm(int variant) {
+int decode_ctas_per_sm(int variant, bool fp8) {
   switch (variant) {
-    case 0: return occupancy_for<1>();
-    case 1: return occupancy_for<2>();
-    default: return occupancy_for<4>();
+    case 0: return fp8 ? occupancy_for<1, true>() : occupancy_for<1, false>();
+    case 1: return fp8 ? occupancy_for<2, true>() : occupancy_for<2, false>();
+    default: return fp8 ? occupancy_for<4, true>() : occupancy_for<4, false>();
   }
 }
 
@@ -882,12 +948,12 @@ size_t attend_workspace_bytes(const DeviceInfo& dev, const pkv_desc& d, int32_t 
       .total;
 }
 
-template <int GH>
+template <int GH, bool F8>
 static int launch_decode(const LaunchCtx& ctx, const DecodeParams& dp) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(dp.nwarps / kDecWarps);
   cfg.blockDim = dim3(kDecThreads);
-  cfg.dynamicSmemBytes = decode_smem_bytes(dp.B);
+  cfg.dynamicSmemBytes = decode_smem_bytes<F8>(dp.B);
   cfg.stream = ctx.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -895,7 +961,7 @@ static int launch_decode(const LaunchCtx& ctx, const DecodeParams& dp) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   TraceScope ts(ctx.stream, PKV_K_DECODE);
-  cudaLaunchKernelEx(&cfg, pkv_decode_kernel<GH>, dp);
+  cudaLaunchKernelEx(&cfg, pkv_decode_kernel<GH, F8>, dp);
   return ts.done();
 }
 
@@ -904,8 +970,11 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   const int G = d.num_q_heads / d.num_kv_heads;
   const int GH = group_per_item(G);
   const int nsub = G / GH;
-  const int nwarps = ctx.dev->dec_warps[variant_of(GH)];
+  // the FP8 variant runs on at most as many warps as the bf16 one, whose count
+  // sizes the workspace
+  const int nwarps = a.fp8 ? ctx.dev->dec_warps_f8[variant_of(GH)] : ctx.dev->dec_warps[variant_of(GH)];
   if (nwarps <= 0) return PKV_ERR_LAUNCH;
+  if (a.fp8 && a.shared_prefix_pages != 0) return PKV_ERR_RANGE;
   if (a.num_seqs > kMaxSeqs) return PKV_ERR_RANGE;
   // unit indices are int32 on the device
   if (int64_t(a.num_tokens) * d.max_blocks_per_seq * d.num_kv_heads * nsub >= (int64_t(1) << 31))
@@ -922,7 +991,8 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   // Long query chunks go to the tensor-core kernel unless the caller's bound
   // says there are none; then split-KV takes every row.
-  const bool prefill = max_tiles > 0 && a.num_tokens > simt_max_q() &&
+  // (FP8 pages: split-KV takes every row)
+  const bool prefill = !a.fp8 && max_tiles > 0 && a.num_tokens > simt_max_q() &&
                        (a.max_query_len <= 0 || a.max_query_len > simt_max_q());
   const int split_max_q = prefill ? simt_max_q() : INT_MAX;
   if (prefill) {
@@ -935,8 +1005,10 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
 
   DecodeParams dp{};
   dp.q = a.q;
-  dp.k_cache = a.k_cache;
-  dp.v_cache = a.v_cache;
+  dp.k_cache = static_cast<const uint8_t*>(a.k_cache);
+  dp.v_cache = static_cast<const uint8_t*>(a.v_cache);
+  dp.k_scale = a.k_scale;
+  dp.v_scale = a.v_scale;
   dp.block_tables = a.block_tables;
   dp.seq_lens = a.seq_lens;
   dp.qsl = a.query_start_loc;
@@ -960,10 +1032,17 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   dp.chunks = chunks;
   dp.prefix_part = reinterpret_cast<const float*>(ws + L.prefix);
 
+  if (a.fp8) {
+    switch (GH) {
+      case 1: return launch_decode<1, true>(ctx, dp);
+      case 2: return launch_decode<2, true>(ctx, dp);
+      default: return launch_decode<4, true>(ctx, dp);
+    }
+  }
   switch (GH) {
-    case 1: return launch_decode<1>(ctx, dp);
-    case 2: return launch_decode<2>(ctx, dp);
-    default: return launch_decode<4>(ctx, dp);
+    case 1: return launch_decode<1, false>(ctx, dp);
+    case 2: return launch_decode<2, false>(ctx, dp);
+    default: return launch_decode<4, false>(ctx, dp);
   }
 }
 

@@ -16,6 +16,7 @@ struct DeviceInfo {
   // Decode warps of one persistent launch, per kernel variant: index 0, 1, 2
   // for 1, 2, 4 query heads sharing a page read.
   int dec_warps[3] = {0, 0, 0};
+  int dec_warps_f8[3] = {0, 0, 0};  // FP8-page variant, never above dec_warps
   size_t smem_optin = 0;
 };
 
@@ -49,11 +50,15 @@ class TraceScope {
 int launch_write(const LaunchCtx& ctx, const uint16_t* k_new, const uint16_t* v_new,
                  const int64_t* slot_mapping, int64_t num_tokens, uint16_t* k_cache,
                  uint16_t* v_cache, int32_t num_blocks, int32_t num_kv_heads);
+int launch_write_fp8(const LaunchCtx& ctx, const uint16_t* k_new, const uint16_t* v_new,
+                     const int64_t* slot_mapping, int64_t num_tokens, uint8_t* k_cache,
+                     uint8_t* v_cache, uint8_t* k_scale, uint8_t* v_scale, int32_t num_blocks,
+                     int32_t num_kv_heads);
 
 struct AttendArgs {
   const uint16_t* q;
-  const uint16_t* k_cache;
-  const uint16_t* v_cache;
+  const void* k_cache;  // bf16 pages, or E4M3 codes when fp8
+  const void* v_cache;
   const int32_t* block_tables;
   const int32_t* seq_lens;
   const int32_t* query_start_loc;
@@ -63,6 +68,9 @@ struct AttendArgs {
   void* workspace;
   size_t workspace_bytes;
   pkv_desc desc;
+  bool fp8 = false;                 // E4M3 pages with per-row scale bytes
+  const uint8_t* k_scale = nullptr;  // [NB][Hkv][16], fp8 only
+  const uint8_t* v_scale = nullptr;
 };
 
 // Workspace bytes for a batch on the current device.
@@ -71,7 +79,7 @@ size_t attend_workspace_bytes(const DeviceInfo& dev, const pkv_desc& d, int32_t 
 int launch_attend(const LaunchCtx& ctx, const AttendArgs& a);
 
 // Resident CTAs per SM of the decode kernel variant (occupancy query).
-int decode_ctas_per_sm(int variant);
+int decode_ctas_per_sm(int variant, bool fp8);
 
 // Tensor-core chunked-prefill path (pkv_prefill.cu).
 int prefill_max_tiles(const pkv_desc& d, int32_t num_seqs, int32_t num_tokens);

@@ -184,13 +184,40 @@ def workload(idx, *, device="cpu", with_tensors=True):
     return b
 
 
-def kv_bytes(batch: Batch, unique: bool = True) -> int:
+# Scale byte of the pre-filled FP8 pool: 2^(121 - 127) = 1/64.
+FP8_FILL_SCALE_BYTE = 121
+
+
+def fp8_pools(batch: Batch, seed: int):
+    """A pre-filled FP8 page pool for ``batch``: E4M3 codes [NB, Hkv, P, D]
+    (uint8) of N(0, 1) * 64 values (clipped to the format's +-448, which
+    N(0, 1) reaches only beyond 7 sigma) and a constant scale byte
+    FP8_FILL_SCALE_BYTE [NB, Hkv, P] (uint8), so the pool holds values close
+    to N(0, 1).  Codes come from torch's float8_e4m3fn conversion with a
+    torch.Generator seeded with ``seed``, on the batch's device.  No per-row
+    scaling: that is the write step's arithmetic, done only by the write
+    under test.  Returns (k_codes, v_codes, k_scale, v_scale)."""
+    dev = batch.q.device if batch.q is not None else torch.device("cpu")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    shape = (batch.num_blocks, batch.num_kv_heads, batch.page_size, batch.head_dim)
+    out = []
+    for _ in range(2):
+        x = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32) * 64.0
+        out.append(x.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8))
+    sc = torch.full(shape[:3], FP8_FILL_SCALE_BYTE, dtype=torch.uint8, device=dev)
+    return out[0], out[1], sc, sc.clone()
+
+
+def kv_bytes(batch: Batch, unique: bool = True, fp8: bool = False) -> int:
     """Bytes of K+V rows a step must read: tokens < L of each sequence.
 
     unique=True counts a page shared by several block tables once (the bytes
-    the method has to move); unique=False counts it once per reader.
+    the method has to move); unique=False counts it once per reader.  fp8:
+    rows of E4M3 codes plus one scale byte each.
     """
-    P, row = batch.page_size, 2 * batch.num_kv_heads * batch.head_dim * 2
+    P = batch.page_size
+    row = 2 * batch.num_kv_heads * (batch.head_dim + 1 if fp8 else batch.head_dim * 2)
     if not unique:
         return int(batch.seq_lens.astype(np.int64).sum()) * row
     seen = {}
