@@ -29,6 +29,11 @@ constexpr int kScaleBytes = kPage;                // FP8 row scales of one (page
 #endif
 constexpr int kDecWarps = PKV_DEC_WARPS;    // warps per CTA
 constexpr int kDecStages = PKV_DEC_STAGES;  // pages (K+V) in flight per warp
+#ifndef PKV_DEC_STAGES_F8
+#define PKV_DEC_STAGES_F8 5
+#endif
+// FP8 pages are half the bytes, so a warp keeps more of them in flight
+constexpr int kDecStagesF8 = PKV_DEC_STAGES_F8;
 constexpr int kMaxGroupPerItem = 4;  // query heads sharing one page read
 
 // A decode partial state of one warp: m[4], l[4], then o[heads][128] (fp32).

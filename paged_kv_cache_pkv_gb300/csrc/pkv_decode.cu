@@ -33,12 +33,22 @@
 //    even/odd tokens, packed fp32x2 FMAs; probabilities are broadcast through
 //    shared memory as (p, p) pairs.
 //  * FP8 pages (template flag F8): the unit moves a 2 KiB K page and a 2 KiB V
-//    page of E4M3 codes plus their 16-byte blocks of per-row scale bytes
-//    (scale = 2^(byte-127)).  Codes are widened exactly (e4m3 -> f16 -> f32);
-//    the K row scale multiplies the finished score, the V row scale the
-//    probability that weights the row, so no per-element scaling is needed.
-//    A lane then reads 16 consecutive codes of a K row (dims 16c..16c+15) and
-//    8 of a V row, which keeps the shared-memory reads conflict free.
+//    page of E4M3 codes (TMA tensor copies with 128-byte swizzle, so the
+//    fragment reads below are bank-conflict free) plus their 16-byte blocks
+//    of per-row scale bytes (scale = 2^(byte-127)).  Widening each code costs
+//    as much as the math it feeds on CUDA cores, so the page's two small
+//    products run as mma.sync m16n8k16 (f16 in, f32 accumulate) straight
+//    from registers: S^T[16 tokens x 8 heads] = K . Q^T with the codes
+//    widened exactly to f16 (E4M3 is a subset of f16) and q scaled by a power
+//    of two into f16 range (exact), then O^T[128 dims x 8 heads] += V^T . P^T
+//    with P in f16.  The contraction index of both products is permuted so
+//    that every lane's operands are whole 16-byte rows of shared memory.
+//    Row scales: the K one multiplies the finished score; the V one weights
+//    the probability relative to the largest V scale seen in the segment
+//    (kept as a running exponent, like the softmax maximum).  A tcgen05 MMA
+//    needs M >= 64 and operands in shared memory; this product has M = 16
+//    and its operands are converted in registers, so the warp-level MMA is
+//    the fit.
 //  * A warp that sees a whole (row, head group) writes bf16 output directly.
 //    A split one writes (m, l, o) to one of its two partial slots and bumps
 //    an epoch-tagged arrival counter; the last warp to arrive merges the
@@ -51,7 +61,6 @@
 #include <type_traits>
 
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
@@ -90,22 +99,71 @@ constexpr int kPageBytesOf = F8 ? kPageBytesF8 : kPageBytes;
 
 // One warp's page ring.
 template <bool F8>
-struct __align__(128) DecRing {
-  uint4 kv[kDecStages][2][kPageBytesOf<F8> / 16];  // [stage][K|V][16 rows]
-  uint4 sc[kDecStages][F8 ? 2 : 1];                // FP8: K and V row scales
-  float2 ps[kPage * kMaxGroupPerItem];              // (p, p) pairs [token][head]
+struct DecRing;
+template <>
+struct __align__(128) DecRing<false> {
+  uint4 kv[kDecStages][2][kPageBytes / 16];  // [stage][K|V][16 rows x 16 vec]
+  float2 ps[kPage * kMaxGroupPerItem];        // (p, p) pairs [token][head]
   StageDesc desc[kDecStages];
   uint64_t bar[kDecStages];
 };
+template <>
+struct __align__(1024) DecRing<true> {
+  uint8_t kv[kDecStagesF8][2][kPageBytesF8];  // 128-byte-swizzled [16 rows][128 codes]
+  uint4 sc[kDecStagesF8][2];                  // K and V row scale bytes
+  float ot[kMaxGroupPerItem * kHeadDim];      // O transposed at a segment's end
+  StageDesc desc[kDecStagesF8];
+  uint64_t bar[kDecStagesF8];
+};
 
-// Exact widening of two E4M3 codes (low byte first) to floats.
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
-  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
-  return __half22float2(*reinterpret_cast<const __half2*>(&r));
+// 2^(byte - 127) for a scale byte in [1, 254]; 0 for byte 0.
+__device__ __forceinline__ float scale_of(uint32_t byte) { return __uint_as_float(byte << 23); }
+
+// Exact widening of the four E4M3 codes of a word to two f16x2 words: bytes
+// 0, 1 -> lo (byte 0 in the low half), bytes 2, 3 -> hi.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
-// 2^(byte - 127) for a scale byte in [1, 254].
-__device__ __forceinline__ float scale_of(uint32_t byte) { return __uint_as_float(byte << 23); }
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// D += A . B, m16n8k16, f16 operands, f32 accumulators (warp-collective).
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Bytes t and t+8 (t < 8) of a 16-byte vector, as two scale bytes.
+__device__ __forceinline__ void bytes_t_t8(const uint4& v, int t, uint32_t& b0, uint32_t& b1) {
+  const int sh = (t & 3) * 8;
+  b0 = (((t & 4) ? v.y : v.x) >> sh) & 0xFFu;
+  b1 = (((t & 4) ? v.w : v.z) >> sh) & 0xFFu;
+}
+
+// 16-byte chunk c of row r of a page copied with 128-byte swizzle.
+__device__ __forceinline__ const uint4& swz(const uint8_t* page, int r, int c) {
+  return *reinterpret_cast<const uint4*>(page + r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// 2D TMA tile load with an L2 cache hint.
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int c0, int c1,
+                                                 uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr float kTau = 8.0f;  // log2-domain slack before the running max moves
@@ -310,21 +368,30 @@ __device__ __forceinline__ void merge_item(const DecodeParams& p, int lane, int 
   }
 }
 
+// tmk / tmv: TMA descriptors of the FP8 pools viewed as [rows][128 codes]
+// (unused by the bf16 variant).
 template <int GH, bool F8>
-__global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS)
+    pkv_decode_kernel(DecodeParams p, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
   using Ring = DecRing<F8>;
-  Ring& R = reinterpret_cast<Ring*>(smem_raw)[wib];
-  int* s_start = reinterpret_cast<int*>(smem_raw + sizeof(Ring) * kDecWarps);
+  constexpr int NS = F8 ? kDecStagesF8 : kDecStages;  // ring stages
+  // the swizzled FP8 pages need 1024-byte aligned stages
+  uint8_t* smem = F8 ? reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                  ~uintptr_t(1023))
+                     : smem_raw;
+  Ring& R = reinterpret_cast<Ring*>(smem)[wib];
+  int* s_start = reinterpret_cast<int*>(smem + sizeof(Ring) * kDecWarps);
   int* s_q0 = s_start + (p.B + 1);
   int* s_len = s_q0 + (p.B + 1);
   const SeqSmem sq{s_start, s_q0, s_len};
   __shared__ int s_wsum[kDecWarps];
 
   if (lane == 0) {
-    for (int s = 0; s < kDecStages; ++s) mbar_init(&R.bar[s], 1);
+    for (int s = 0; s < NS; ++s) mbar_init(&R.bar[s], 1);
     fence_mbar_init();
   }
   // Under programmatic dependent launch everything up to griddep_wait() below
@@ -422,17 +489,21 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
       const size_t ph = size_t(pc.bid) * p.Hkv + g;  // (page, kv head)
       R.desc[stage] = StageDesc{pc.q0 + pc.j, pc.item, pc.item_start, pc.nvis - p.np * kPage};
       mbar_arrive_expect_tx(&R.bar[stage], 2 * PB + (F8 ? 2 * kScaleBytes : 0));
-      bulk_g2s(&R.kv[stage][0][0], p.k_cache + ph * PB, PB, &R.bar[stage], policy);
-      bulk_g2s(&R.kv[stage][1][0], p.v_cache + ph * PB, PB, &R.bar[stage], policy);
       if constexpr (F8) {
+        const int row0 = int(ph) * kPage;  // the host checks that rows fit int32
+        tma_load_2d_hint(&R.kv[stage][0][0], &tmk, 0, row0, &R.bar[stage], policy);
+        tma_load_2d_hint(&R.kv[stage][1][0], &tmv, 0, row0, &R.bar[stage], policy);
         bulk_g2s(&R.sc[stage][0], p.k_scale + ph * kScaleBytes, kScaleBytes, &R.bar[stage], policy);
         bulk_g2s(&R.sc[stage][1], p.v_scale + ph * kScaleBytes, kScaleBytes, &R.bar[stage], policy);
+      } else {
+        bulk_g2s(&R.kv[stage][0][0], p.k_cache + ph * PB, PB, &R.bar[stage], policy);
+        bulk_g2s(&R.kv[stage][1][0], p.v_cache + ph * PB, PB, &R.bar[stage], policy);
       }
     }
   };
   griddep_wait();
   {
-    const int prologue = min(kDecStages, n_units);
+    const int prologue = min(NS, n_units);
     for (int s = 0; s < prologue; ++s) {
       issue(s);
       if (s + 1 < n_units) cursor_advance(pc, p, sq, per_row);
@@ -451,6 +522,17 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
   float2 o[GH][4];   // dims 8dc+2e, 8dc+2e+1
   float m[GH];
   float lsum[NVL];
+  // FP8 (MMA fragments): lane = (gq = lane/4, tq = lane%4).  qb: Q^T operand
+  // of head gq, dims 32tq+4s+{0,1} / {2,3} for k-step s; oacc: O^T of dims
+  // 16gq+2mb+{0,1} (M-block mb) for heads 2tq, 2tq+1; m2 / l2 the running
+  // maximum and sum of those two heads over this lane's tokens gq, gq+8.
+  const int gq = lane >> 2, tq = lane & 3;
+  uint32_t qb[8][2];
+  float oacc[8][4];
+  float m2[2], l2[2];
+  float qmul = 0.f;   // scale * log2(e) * 2^-kq
+  int eref = 0;       // largest V scale byte of the segment so far (0: none)
+  float lfin[GH];     // FP8: per-head sums, ready for the flush
   int cur_row = -1, cur_item = -1, cur_item_start = 0, cur_seg_start = 0, cur_nvis = 0, cur_h0 = 0;
 
   auto start_segment = [&](const StageDesc& d, int u) {
@@ -462,26 +544,107 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
     const int g = d.item / p.nsub, sub = d.item - g * p.nsub;
     cur_h0 = g * p.G + sub * GH;
     const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (size_t(d.row) * p.Hq + cur_h0) * kHeadDim);
+    if constexpr (F8) {
+      // head gq's dims 32tq..32tq+31 (zero for heads past the group)
+      float qv[32];
+      float amax = 0.f;
 #pragma unroll
-    for (int h = 0; h < GH; ++h) {
-      // the lane's dims: {8c..8c+7, 64+8c..64+8c+7} (bf16), 16c..16c+15 (FP8)
-      const uint4 a = __ldg(qrow + h * 16 + (F8 ? 2 * c8 : c8));
-      const uint4 b = __ldg(qrow + h * 16 + (F8 ? 2 * c8 + 1 : 8 + c8));
-      const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+      for (int c = 0; c < 4; ++c) {
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if (gq < GH) x = __ldg(qrow + gq * 16 + tq * 4 + c);
+        const uint32_t wq[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        qf[h][e] = make_float2(bf_lo(wa[e]) * p.qscale, bf_hi(wa[e]) * p.qscale);
-        qf[h][4 + e] = make_float2(bf_lo(wb[e]) * p.qscale, bf_hi(wb[e]) * p.qscale);
+        for (int e = 0; e < 4; ++e) {
+          qv[c * 8 + 2 * e] = bf_lo(wq[e]);
+          qv[c * 8 + 2 * e + 1] = bf_hi(wq[e]);
+          amax = fmaxf(amax, fmaxf(fabsf(qv[c * 8 + 2 * e]), fabsf(qv[c * 8 + 2 * e + 1])));
+        }
       }
-      m[h] = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) o[h][e] = make_float2(0.f, 0.f);
+      for (int o2 = 1; o2 < 32; o2 <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o2));
+      // power of two that puts the group's largest |q| in [2^14, 2^15): exact in f16
+      int kq = 0;
+      if (amax > 0.f) kq = 14 - (int((__float_as_uint(amax) >> 23) & 0xFF) - 127);
+      kq = max(-100, min(kq, 64));
+      const float up = __uint_as_float(uint32_t(127 + kq) << 23);
+      qmul = p.qscale * __uint_as_float(uint32_t(127 - kq) << 23);
+#pragma unroll
+      for (int st = 0; st < 8; ++st) {
+        qb[st][0] = pack_f16x2(qv[4 * st] * up, qv[4 * st + 1] * up);
+        qb[st][1] = pack_f16x2(qv[4 * st + 2] * up, qv[4 * st + 3] * up);
+      }
+#pragma unroll
+      for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oacc[mb][e] = 0.f;
+      m2[0] = m2[1] = -INFINITY;
+      l2[0] = l2[1] = 0.f;
+      eref = 0;
+#pragma unroll
+      for (int k = 0; k < NVL; ++k) lsum[k] = 0.f;
+    } else {
+#pragma unroll
+      for (int h = 0; h < GH; ++h) {
+        // the lane's dims: {8c..8c+7, 64+8c..64+8c+7}
+        const uint4 a = __ldg(qrow + h * 16 + c8);
+        const uint4 b = __ldg(qrow + h * 16 + 8 + c8);
+        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          qf[h][e] = make_float2(bf_lo(wa[e]) * p.qscale, bf_hi(wa[e]) * p.qscale);
+          qf[h][4 + e] = make_float2(bf_lo(wb[e]) * p.qscale, bf_hi(wb[e]) * p.qscale);
+        }
+        m[h] = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[h][e] = make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < NVL; ++k) lsum[k] = 0.f;
     }
-#pragma unroll
-    for (int k = 0; k < NVL; ++k) lsum[k] = 0.f;
+  };
+
+  // FP8: bring the MMA-fragment state into the layout of the split-KV path
+  // (o by (dc, par) lanes, m and l of every head on every lane).
+  auto f8_to_common = [&]() {
+    if constexpr (F8) {
+      const float os = scale_of(uint32_t(eref));
+  #pragma unroll
+      for (int mb = 0; mb < 8; ++mb) {
+        const int d0 = 16 * gq + 2 * mb;
+        if (2 * tq < GH) {
+          R.ot[(2 * tq) * kHeadDim + d0] = oacc[mb][0] * os;
+          R.ot[(2 * tq) * kHeadDim + d0 + 1] = oacc[mb][2] * os;
+        }
+        if (2 * tq + 1 < GH) {
+          R.ot[(2 * tq + 1) * kHeadDim + d0] = oacc[mb][1] * os;
+          R.ot[(2 * tq + 1) * kHeadDim + d0 + 1] = oacc[mb][3] * os;
+        }
+      }
+      __syncwarp();
+  #pragma unroll
+      for (int h = 0; h < GH; ++h)
+  #pragma unroll
+        for (int e = 0; e < 4; ++e)
+          o[h][e] = par == 0 ? *reinterpret_cast<const float2*>(&R.ot[h * kHeadDim + 8 * dc + 2 * e])
+                             : make_float2(0.f, 0.f);
+      __syncwarp();
+      float lr[2] = {l2[0], l2[1]};
+  #pragma unroll
+      for (int k = 0; k < 2; ++k)
+  #pragma unroll
+        for (int o2 = 4; o2 < 32; o2 <<= 1) lr[k] += __shfl_xor_sync(kFull, lr[k], o2);
+  #pragma unroll
+      for (int h = 0; h < GH; ++h) {
+        const float mh0 = __shfl_sync(kFull, m2[0], h >> 1), mh1 = __shfl_sync(kFull, m2[1], h >> 1);
+        const float lh0 = __shfl_sync(kFull, lr[0], h >> 1), lh1 = __shfl_sync(kFull, lr[1], h >> 1);
+        m[h] = (h & 1) ? mh1 : mh0;
+        lfin[h] = (h & 1) ? lh1 : lh0;
+      }
+    }
   };
 
   auto flush_segment = [&]() {
+    if constexpr (F8) f8_to_common();
 #pragma unroll
     for (int h = 0; h < GH; ++h)
 #pragma unroll
@@ -500,7 +663,10 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
       lpart[k] = x;
     }
     float l[GH];
-    if constexpr (GH == 4) {
+    if constexpr (F8) {
+#pragma unroll
+      for (int h = 0; h < GH; ++h) l[h] = lfin[h];
+    } else if constexpr (GH == 4) {
       const float x0 = __shfl_xor_sync(kFull, lpart[0], 1), x1 = __shfl_xor_sync(kFull, lpart[1], 1);
       l[0] = h3 ? x0 : lpart[0];
       l[1] = h3 ? x1 : lpart[1];
@@ -645,8 +811,8 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
   bool timed_out = false;
   int it = 0;
   for (; it < n_units; ++it) {
-    const int stage = it % kDecStages;
-    const uint32_t parity = (it / kDecStages) & 1;
+    const int stage = it % NS;
+    const uint32_t parity = (it / NS) & 1;
     if (!mbar_wait(&R.bar[stage], parity)) {
       timed_out = true;
       break;
@@ -659,207 +825,321 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
     }
     const int j = u - d.item_start;
     const int nvalid = min(kPage, d.nvis - j * kPage);
-    const uint4* Ks = R.kv[stage][0];
-    const uint4* Vs = R.kv[stage][1];
-
-    // ---- V slice of this lane into registers (even/odd tokens x 8 dims) ----
-    using VVec = std::conditional_t<F8, uint2, uint4>;  // 8 dims of one row
-    VVec vreg[kPage / 2];
-#pragma unroll
-    for (int i = 0; i < kPage / 2; ++i)
-      vreg[i] = reinterpret_cast<const VVec*>(Vs)[(par + 2 * i) * 16 + dc];
-    // FP8: the row scales of this lane's score token, read before the stage
-    // goes back to the copy engine
-    float kscale = 1.f, vscale = 1.f;
     if constexpr (F8) {
-      const uint8_t* sc = reinterpret_cast<const uint8_t*>(&R.sc[stage][0]);
-      kscale = scale_of(sc[my_tok]);
-      vscale = scale_of(sc[kScaleBytes + my_tok]);
-    }
+      // ---- operands of this lane out of the swizzled stage ----
+      const uint8_t* Kp = R.kv[stage][0];
+      const uint8_t* Vp = R.kv[stage][1];
+      // K rows gq and gq+8, codes of dims 32tq..32tq+31 (chunks 2tq, 2tq+1)
+      const uint4 ka0 = swz(Kp, gq, 2 * tq), ka1 = swz(Kp, gq, 2 * tq + 1);
+      const uint4 kb0 = swz(Kp, gq + 8, 2 * tq), kb1 = swz(Kp, gq + 8, 2 * tq + 1);
+      // V rows 2tq, 2tq+1, 2tq+8, 2tq+9, codes of dims 16gq..16gq+15 (chunk gq)
+      uint4 va = swz(Vp, 2 * tq, gq), vb = swz(Vp, 2 * tq + 1, gq);
+      uint4 vc = swz(Vp, 2 * tq + 8, gq), vd = swz(Vp, 2 * tq + 9, gq);
+      const uint4 ksc = R.sc[stage][0], vsc = R.sc[stage][1];
+      // The page now lives in registers: hand the stage back to the copy engine.
+      __syncwarp();
+      if (it + NS < n_units) {
+        issue(stage);
+        if (it + NS + 1 < n_units) cursor_advance(pc, p, sq, per_row);
+      }
 
-    // ---- scores: 4 tokens x GH heads per lane, partial over 16 dims ----
-    float v[4 * GH];
+      // ---- S^T = K . Q^T: 8 k-steps of 16 (permuted) dims ----
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        // two accumulator chains (even / odd k-steps) halve the MMA latency chain
+        float sodd[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t wa[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
+        const uint32_t wb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t = grp + 4 * i;
-      float2 kf[8];
-      if constexpr (F8) {
-        const uint4 a = Ks[t * 8 + c8];  // codes of dims 16c..16c+15
-        const uint32_t wk[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          kf[2 * e] = e4m3x2_to_float2(wk[e] & 0xFFFFu);
-          kf[2 * e + 1] = e4m3x2_to_float2(wk[e] >> 16);
+        for (int st = 0; st < 8; ++st) {
+          uint32_t a0, a1, a2, a3;
+          e4m3x4_to_f16x2(wa[st], a0, a2);
+          e4m3x4_to_f16x2(wb[st], a1, a3);
+          mma_f16((st & 1) ? sodd : sacc, a0, a1, a2, a3, qb[st][0], qb[st][1]);
         }
-      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[e] += sodd[e];
+      }
+      // scores (log2 domain) of tokens gq, gq+8 for heads 2tq, 2tq+1
+      const bool t0 = gq < nvalid, t1 = gq + 8 < nvalid;
+      const bool h0 = 2 * tq < GH, h1r = 2 * tq + 1 < GH;
+      uint32_t kb_0, kb_1, vb_0, vb_1;
+      bytes_t_t8(ksc, gq, kb_0, kb_1);
+      bytes_t_t8(vsc, gq, vb_0, vb_1);
+      const float f0 = qmul * scale_of(kb_0), f1 = qmul * scale_of(kb_1);
+      float sv[4];
+      sv[0] = t0 && h0 ? sacc[0] * f0 : -INFINITY;
+      sv[1] = t0 && h1r ? sacc[1] * f0 : -INFINITY;
+      sv[2] = t1 && h0 ? sacc[2] * f1 : -INFINITY;
+      sv[3] = t1 && h1r ? sacc[3] * f1 : -INFINITY;
+
+      // largest V scale byte among the page's valid rows
+      uint32_t vmax;
+      {
+        uint32_t w4[4] = {vsc.x, vsc.y, vsc.z, vsc.w};
+        if (nvalid < kPage) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int keep = min(4, max(0, nvalid - 4 * q4));  // valid bytes in this word
+            w4[q4] &= keep >= 4 ? 0xFFFFFFFFu : ((1u << (8 * keep)) - 1u);
+          }
+        }
+        const uint32_t x = __vmaxu4(__vmaxu4(w4[0], w4[1]), __vmaxu4(w4[2], w4[3]));
+        const uint32_t y = __vmaxu4(x, x >> 16);
+        vmax = max(y & 0xFFu, (y >> 8) & 0xFFu);
+      }
+
+      // ---- lazy running maximum (and the V-scale reference) ----
+      bool exceed = sv[0] > m2[0] + kTau || sv[2] > m2[0] + kTau || sv[1] > m2[1] + kTau ||
+                    sv[3] > m2[1] + kTau;
+      const bool grow = int(vmax) > eref;  // warp-uniform
+      if (__any_sync(kFull, exceed) || grow) {
+        float full0 = fmaxf(sv[0], sv[2]), full1 = fmaxf(sv[1], sv[3]);
+#pragma unroll
+        for (int o2 = 4; o2 < 32; o2 <<= 1) {
+          full0 = fmaxf(full0, __shfl_xor_sync(kFull, full0, o2));
+          full1 = fmaxf(full1, __shfl_xor_sync(kFull, full1, o2));
+        }
+        const float mn0 = fmaxf(m2[0], full0), mn1 = fmaxf(m2[1], full1);
+        float a0 = m2[0] == -INFINITY ? 0.f : ex2(m2[0] - mn0);
+        float a1 = m2[1] == -INFINITY ? 0.f : ex2(m2[1] - mn1);
+        m2[0] = mn0;
+        m2[1] = mn1;
+        l2[0] *= a0;
+        l2[1] *= a1;
+        if (grow) {
+          // O was weighted relative to 2^(eref-127); move it to the new reference
+          const int dlt = eref - int(vmax) + 127;
+          const float b = dlt >= 1 ? scale_of(uint32_t(dlt)) : 0.f;
+          a0 *= b;
+          a1 *= b;
+          eref = int(vmax);
+        }
+#pragma unroll
+        for (int mb = 0; mb < 8; ++mb) {
+          oacc[mb][0] *= a0;
+          oacc[mb][1] *= a1;
+          oacc[mb][2] *= a0;
+          oacc[mb][3] *= a1;
+        }
+      }
+
+      // ---- probabilities, weighted by 2^(V scale - reference) for the PV product ----
+      const float r0 = m2[0] == -INFINITY ? 0.f : m2[0], r1 = m2[1] == -INFINITY ? 0.f : m2[1];
+      const float p0 = ex2(sv[0] - r0), p1 = ex2(sv[1] - r1), p2 = ex2(sv[2] - r0), p3 = ex2(sv[3] - r1);
+      l2[0] += p0 + p2;
+      l2[1] += p1 + p3;
+      float w0 = 0.f, w1 = 0.f;
+      if (t0) {
+        const int dl = int(vb_0) - eref + 127;
+        w0 = dl >= 1 ? scale_of(uint32_t(dl)) : 0.f;
+      }
+      if (t1) {
+        const int dl = int(vb_1) - eref + 127;
+        w1 = dl >= 1 ? scale_of(uint32_t(dl)) : 0.f;
+      }
+      // this lane's P for its even head (2tq) and odd head (2tq+1): tokens gq, gq+8
+      const uint32_t pe = pack_f16x2(p0 * w0, p2 * w1), po = pack_f16x2(p1 * w0, p3 * w1);
+      // P^T operand: head gq, tokens 2tq, 2tq+1 (b0) and 2tq+8, 2tq+9 (b1),
+      // gathered from the lanes that hold those tokens for head pair gq/2
+      const int src0 = 8 * tq + (gq >> 1), src1 = src0 + 4;
+      const uint32_t x0 = __shfl_sync(kFull, pe, src0), x1 = __shfl_sync(kFull, po, src0);
+      const uint32_t y0 = __shfl_sync(kFull, pe, src1), y1 = __shfl_sync(kFull, po, src1);
+      const uint32_t X = (gq & 1) ? x1 : x0, Y = (gq & 1) ? y1 : y0;
+      uint32_t pb0 = __byte_perm(X, Y, 0x5410), pb1 = __byte_perm(X, Y, 0x7632);
+      if (gq >= GH) pb0 = pb1 = 0u;
+
+      // ---- O^T += V^T . P^T: 8 M-blocks of 16 (permuted) dims ----
+      if (nvalid < kPage) {  // rows past the sequence may hold anything (NaN)
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        if (2 * tq >= nvalid) va = z;
+        if (2 * tq + 1 >= nvalid) vb = z;
+        if (2 * tq + 8 >= nvalid) vc = z;
+        if (2 * tq + 9 >= nvalid) vd = z;
+      }
+      const uint32_t A4[4] = {va.x, va.y, va.z, va.w}, B4[4] = {vb.x, vb.y, vb.z, vb.w};
+      const uint32_t C4[4] = {vc.x, vc.y, vc.z, vc.w}, D4[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+      for (int mb = 0; mb < 8; ++mb) {
+        const uint32_t sel = (mb & 1) ? 0x7362u : 0x5140u;
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16x2(__byte_perm(A4[mb >> 1], B4[mb >> 1], sel), a0, a1);
+        e4m3x4_to_f16x2(__byte_perm(C4[mb >> 1], D4[mb >> 1], sel), a2, a3);
+        mma_f16(oacc[mb], a0, a1, a2, a3, pb0, pb1);
+      }
+    } else {
+
+      const uint4* Ks = R.kv[stage][0];
+      const uint4* Vs = R.kv[stage][1];
+
+      // ---- V slice of this lane into registers (even/odd tokens x 8 dims) ----
+      uint4 vreg[kPage / 2];
+#pragma unroll
+      for (int i = 0; i < kPage / 2; ++i) vreg[i] = Vs[(par + 2 * i) * 16 + dc];
+
+      // ---- scores: 4 tokens x GH heads per lane, partial over 16 dims ----
+      float v[4 * GH];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = grp + 4 * i;
         const uint4 a = Ks[t * 16 + c8];
         const uint4 b = Ks[t * 16 + 8 + c8];
         const uint32_t wk[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float2 kf[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) kf[e] = make_float2(bf_lo(wk[e]), bf_hi(wk[e]));
-      }
 #pragma unroll
-      for (int h = 0; h < GH; ++h) {
-        float2 acc = __fmul2_rn(qf[h][0], kf[0]);
+        for (int h = 0; h < GH; ++h) {
+          float2 acc = __fmul2_rn(qf[h][0], kf[0]);
 #pragma unroll
-        for (int e = 1; e < 8; ++e) acc = __ffma2_rn(qf[h][e], kf[e], acc);
-        v[i * GH + h] = acc.x + acc.y;
-      }
-    }
-    // The page now lives in registers: hand the stage back to the copy engine.
-    __syncwarp();
-    if (it + kDecStages < n_units) {
-      issue(stage);
-      if (it + kDecStages + 1 < n_units) cursor_advance(pc, p, sq, per_row);
-    }
-
-    // transposing butterfly over lanes xor 4, 2, 1
-    {
-      constexpr int N0 = 4 * GH;
-#pragma unroll
-      for (int i = 0; i < N0 / 2; ++i) {
-        const float a = v[i], b = v[i + N0 / 2];
-        const float send = h1 ? a : b, keep = h1 ? b : a;
-        v[i] = keep + __shfl_xor_sync(kFull, send, 4);
-      }
-      constexpr int N1 = N0 / 2;
-#pragma unroll
-      for (int i = 0; i < N1 / 2; ++i) {
-        const float a = v[i], b = v[i + N1 / 2];
-        const float send = h2 ? a : b, keep = h2 ? b : a;
-        v[i] = keep + __shfl_xor_sync(kFull, send, 2);
-      }
-      constexpr int N2 = N1 / 2;
-      if constexpr (N2 >= 2) {
-#pragma unroll
-        for (int i = 0; i < N2 / 2; ++i) {
-          const float a = v[i], b = v[i + N2 / 2];
-          const float send = h3 ? a : b, keep = h3 ? b : a;
-          v[i] = keep + __shfl_xor_sync(kFull, send, 1);
+          for (int e = 1; e < 8; ++e) acc = __ffma2_rn(qf[h][e], kf[e], acc);
+          v[i * GH + h] = acc.x + acc.y;
         }
-      } else {
-        v[0] += __shfl_xor_sync(kFull, v[0], 1);
       }
-    }
-    float s[NVL];
-#pragma unroll
-    for (int k = 0; k < NVL; ++k) s[k] = my_tok < nvalid ? v[k] * kscale : -INFINITY;
+      // The page now lives in registers: hand the stage back to the copy engine.
+      __syncwarp();
+      if (it + NS < n_units) {
+        issue(stage);
+        if (it + NS + 1 < n_units) cursor_advance(pc, p, sq, per_row);
+      }
 
-    // ---- online softmax (log2 domain) ----
-    float mine[NVL];
+      // transposing butterfly over lanes xor 4, 2, 1
+      {
+        constexpr int N0 = 4 * GH;
 #pragma unroll
-    for (int k = 0; k < NVL; ++k) {
-      float mm = m[0];
+        for (int i = 0; i < N0 / 2; ++i) {
+          const float a = v[i], b = v[i + N0 / 2];
+          const float send = h1 ? a : b, keep = h1 ? b : a;
+          v[i] = keep + __shfl_xor_sync(kFull, send, 4);
+        }
+        constexpr int N1 = N0 / 2;
 #pragma unroll
-      for (int x = 0; x < GH; ++x)
-        if (x == head_of(k)) mm = m[x];
-      mine[k] = mm;
-    }
-    bool exceed = false;
+        for (int i = 0; i < N1 / 2; ++i) {
+          const float a = v[i], b = v[i + N1 / 2];
+          const float send = h2 ? a : b, keep = h2 ? b : a;
+          v[i] = keep + __shfl_xor_sync(kFull, send, 2);
+        }
+        constexpr int N2 = N1 / 2;
+        if constexpr (N2 >= 2) {
 #pragma unroll
-    for (int k = 0; k < NVL; ++k) exceed |= s[k] > mine[k] + kTau;
-    if (__any_sync(kFull, exceed)) {
-      float pm[NVL];
+          for (int i = 0; i < N2 / 2; ++i) {
+            const float a = v[i], b = v[i + N2 / 2];
+            const float send = h3 ? a : b, keep = h3 ? b : a;
+            v[i] = keep + __shfl_xor_sync(kFull, send, 1);
+          }
+        } else {
+          v[0] += __shfl_xor_sync(kFull, v[0], 1);
+        }
+      }
+      float s[NVL];
+#pragma unroll
+      for (int k = 0; k < NVL; ++k) s[k] = my_tok < nvalid ? v[k] : -INFINITY;
+
+      // ---- online softmax (log2 domain) ----
+      float mine[NVL];
 #pragma unroll
       for (int k = 0; k < NVL; ++k) {
-        float x = s[k];
-        x = fmaxf(x, __shfl_xor_sync(kFull, x, 2));
-        x = fmaxf(x, __shfl_xor_sync(kFull, x, 4));
-        x = fmaxf(x, __shfl_xor_sync(kFull, x, 8));
-        x = fmaxf(x, __shfl_xor_sync(kFull, x, 16));
-        pm[k] = x;
-      }
-      float full[GH];
-      if constexpr (GH == 4) {
-        const float x0 = __shfl_xor_sync(kFull, pm[0], 1), x1 = __shfl_xor_sync(kFull, pm[1], 1);
-        full[0] = h3 ? x0 : pm[0];
-        full[1] = h3 ? x1 : pm[1];
-        full[2] = h3 ? pm[0] : x0;
-        full[3] = h3 ? pm[1] : x1;
-      } else if constexpr (GH == 2) {
-        const float x0 = __shfl_xor_sync(kFull, pm[0], 1);
-        full[0] = h3 ? x0 : pm[0];
-        full[1] = h3 ? pm[0] : x0;
-      } else {
-        full[0] = pm[0];
-      }
-      float alpha[GH];
-#pragma unroll
-      for (int h = 0; h < GH; ++h) {
-        const float mn = fmaxf(m[h], full[h]);
-        alpha[h] = m[h] == -INFINITY ? 0.f : ex2(m[h] - mn);
-        m[h] = mn;
-        const float2 a2 = make_float2(alpha[h], alpha[h]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[h][e] = __fmul2_rn(o[h][e], a2);
-      }
-#pragma unroll
-      for (int k = 0; k < NVL; ++k) {
-        float a = alpha[0], mm = m[0];
+        float mm = m[0];
 #pragma unroll
         for (int x = 0; x < GH; ++x)
-          if (x == head_of(k)) {
-            a = alpha[x];
-            mm = m[x];
-          }
-        lsum[k] *= a;
+          if (x == head_of(k)) mm = m[x];
         mine[k] = mm;
       }
-    }
-    float pr[NVL];
+      bool exceed = false;
 #pragma unroll
-    for (int k = 0; k < NVL; ++k) {
-      pr[k] = ex2(s[k] - mine[k]);
-      lsum[k] += pr[k];
-      // FP8: weight the row's codes by p * 2^(V scale) (masked rows stay 0)
-      if constexpr (F8) pr[k] = my_tok < nvalid ? pr[k] * vscale : 0.f;
-    }
-    if constexpr (GH == 4) {
-      *reinterpret_cast<float4*>(&R.ps[my_tok * 4 + 2 * h3]) = make_float4(pr[0], pr[0], pr[1], pr[1]);
-    } else if constexpr (GH == 2) {
-      R.ps[my_tok * 2 + h3] = make_float2(pr[0], pr[0]);
-    } else {
-      R.ps[my_tok] = make_float2(pr[0], pr[0]);
-    }
-    __syncwarp();
-
-    // ---- PV from registers: even/odd tokens x 8 dims per lane ----
+      for (int k = 0; k < NVL; ++k) exceed |= s[k] > mine[k] + kTau;
+      if (__any_sync(kFull, exceed)) {
+        float pm[NVL];
 #pragma unroll
-    for (int i = 0; i < kPage / 2; ++i) {
-      const int t = par + 2 * i;
-      if (nvalid == kPage || t < nvalid) {
-        float2 vf[4];
-        if constexpr (F8) {
-          const uint32_t wv[2] = {vreg[i].x, vreg[i].y};
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            vf[2 * e] = e4m3x2_to_float2(wv[e] & 0xFFFFu);
-            vf[2 * e + 1] = e4m3x2_to_float2(wv[e] >> 16);
-          }
+        for (int k = 0; k < NVL; ++k) {
+          float x = s[k];
+          x = fmaxf(x, __shfl_xor_sync(kFull, x, 2));
+          x = fmaxf(x, __shfl_xor_sync(kFull, x, 4));
+          x = fmaxf(x, __shfl_xor_sync(kFull, x, 8));
+          x = fmaxf(x, __shfl_xor_sync(kFull, x, 16));
+          pm[k] = x;
+        }
+        float full[GH];
+        if constexpr (GH == 4) {
+          const float x0 = __shfl_xor_sync(kFull, pm[0], 1), x1 = __shfl_xor_sync(kFull, pm[1], 1);
+          full[0] = h3 ? x0 : pm[0];
+          full[1] = h3 ? x1 : pm[1];
+          full[2] = h3 ? pm[0] : x0;
+          full[3] = h3 ? pm[1] : x1;
+        } else if constexpr (GH == 2) {
+          const float x0 = __shfl_xor_sync(kFull, pm[0], 1);
+          full[0] = h3 ? x0 : pm[0];
+          full[1] = h3 ? pm[0] : x0;
         } else {
+          full[0] = pm[0];
+        }
+        float alpha[GH];
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+          const float mn = fmaxf(m[h], full[h]);
+          alpha[h] = m[h] == -INFINITY ? 0.f : ex2(m[h] - mn);
+          m[h] = mn;
+          const float2 a2 = make_float2(alpha[h], alpha[h]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[h][e] = __fmul2_rn(o[h][e], a2);
+        }
+#pragma unroll
+        for (int k = 0; k < NVL; ++k) {
+          float a = alpha[0], mm = m[0];
+#pragma unroll
+          for (int x = 0; x < GH; ++x)
+            if (x == head_of(k)) {
+              a = alpha[x];
+              mm = m[x];
+            }
+          lsum[k] *= a;
+          mine[k] = mm;
+        }
+      }
+      float pr[NVL];
+#pragma unroll
+      for (int k = 0; k < NVL; ++k) {
+        pr[k] = ex2(s[k] - mine[k]);
+        lsum[k] += pr[k];
+      }
+      if constexpr (GH == 4) {
+        *reinterpret_cast<float4*>(&R.ps[my_tok * 4 + 2 * h3]) = make_float4(pr[0], pr[0], pr[1], pr[1]);
+      } else if constexpr (GH == 2) {
+        R.ps[my_tok * 2 + h3] = make_float2(pr[0], pr[0]);
+      } else {
+        R.ps[my_tok] = make_float2(pr[0], pr[0]);
+      }
+      __syncwarp();
+
+      // ---- PV from registers: even/odd tokens x 8 dims per lane ----
+#pragma unroll
+      for (int i = 0; i < kPage / 2; ++i) {
+        const int t = par + 2 * i;
+        if (nvalid == kPage || t < nvalid) {
           const uint32_t wv[4] = {vreg[i].x, vreg[i].y, vreg[i].z, vreg[i].w};
+          float2 vf[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) vf[e] = make_float2(bf_lo(wv[e]), bf_hi(wv[e]));
-        }
-        float2 pv[GH];
-        if constexpr (GH == 4) {
-          const float4 x = *reinterpret_cast<const float4*>(&R.ps[t * 4]);
-          const float4 y = *reinterpret_cast<const float4*>(&R.ps[t * 4 + 2]);
-          pv[0] = make_float2(x.x, x.y);
-          pv[1] = make_float2(x.z, x.w);
-          pv[2] = make_float2(y.x, y.y);
-          pv[3] = make_float2(y.z, y.w);
-        } else if constexpr (GH == 2) {
-          const float4 x = *reinterpret_cast<const float4*>(&R.ps[t * 2]);
-          pv[0] = make_float2(x.x, x.y);
-          pv[1] = make_float2(x.z, x.w);
-        } else {
-          pv[0] = R.ps[t];
-        }
+          float2 pv[GH];
+          if constexpr (GH == 4) {
+            const float4 x = *reinterpret_cast<const float4*>(&R.ps[t * 4]);
+            const float4 y = *reinterpret_cast<const float4*>(&R.ps[t * 4 + 2]);
+            pv[0] = make_float2(x.x, x.y);
+            pv[1] = make_float2(x.z, x.w);
+            pv[2] = make_float2(y.x, y.y);
+            pv[3] = make_float2(y.z, y.w);
+          } else if constexpr (GH == 2) {
+            const float4 x = *reinterpret_cast<const float4*>(&R.ps[t * 2]);
+            pv[0] = make_float2(x.x, x.y);
+            pv[1] = make_float2(x.z, x.w);
+          } else {
+            pv[0] = R.ps[t];
+          }
 #pragma unroll
-        for (int h = 0; h < GH; ++h)
+          for (int h = 0; h < GH; ++h)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) o[h][e] = __ffma2_rn(pv[h], vf[e], o[h][e]);
+            for (int e = 0; e < 4; ++e) o[h][e] = __ffma2_rn(pv[h], vf[e], o[h][e]);
+        }
       }
     }
   }
@@ -867,8 +1147,8 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS) pkv_decode_kern
   if (timed_out) {
     if (lane == 0) flag_status(p.status, PKV_STATUS_TIMEOUT);
     // let copies still in flight land before the CTA's shared memory is released
-    for (int k = it; k < min(n_units, it + kDecStages); ++k)
-      mbar_wait(&R.bar[k % kDecStages], (k / kDecStages) & 1, kDrainLimitNs);
+    for (int k = it; k < min(n_units, it + NS); ++k)
+      mbar_wait(&R.bar[k % NS], (k / NS) & 1, kDrainLimitNs);
     return;
   }
   if (cur_row >= 0) flush_segment();
@@ -884,7 +1164,7 @@ static int variant_of(int gh) { return gh == 4 ? 2 : gh - 1; }
 // ([B+1] each) and seq_lens ([B]).
 template <bool F8>
 static size_t decode_smem_bytes(int num_seqs) {
-  return sizeof(DecRing<F8>) * kDecWarps + sizeof(int) * (3 * size_t(num_seqs) + 2);
+  return (F8 ? 1024 : 0) + sizeof(DecRing<F8>) * kDecWarps + sizeof(int) * (3 * size_t(num_seqs) + 2);
 }
 
 template <int GH, bool F8>
@@ -949,7 +1229,8 @@ size_t attend_workspace_bytes(const DeviceInfo& dev, const pkv_desc& d, int32_t 
 }
 
 template <int GH, bool F8>
-static int launch_decode(const LaunchCtx& ctx, const DecodeParams& dp) {
+static int launch_decode(const LaunchCtx& ctx, const DecodeParams& dp, const CUtensorMap& tk,
+                         const CUtensorMap& tv) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(dp.nwarps / kDecWarps);
   cfg.blockDim = dim3(kDecThreads);
@@ -961,7 +1242,7 @@ static int launch_decode(const LaunchCtx& ctx, const DecodeParams& dp) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   TraceScope ts(ctx.stream, PKV_K_DECODE);
-  cudaLaunchKernelEx(&cfg, pkv_decode_kernel<GH, F8>, dp);
+  cudaLaunchKernelEx(&cfg, pkv_decode_kernel<GH, F8>, dp, tk, tv);
   return ts.done();
 }
 
@@ -1032,17 +1313,27 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   dp.chunks = chunks;
   dp.prefix_part = reinterpret_cast<const float*>(ws + L.prefix);
 
+  CUtensorMap tk{}, tv{};  // unused by the bf16 variant
   if (a.fp8) {
+    // the pools as [rows][128 codes], one 16-row box per (page, kv head)
+    const cuuint64_t rows = cuuint64_t(d.num_blocks) * d.num_kv_heads * kPage;
+    if (rows > cuuint64_t(INT_MAX)) return PKV_ERR_RANGE;  // TMA row coordinates are int32
+    const cuuint64_t dims[2] = {cuuint64_t(kHeadDim), rows};
+    const cuuint64_t strides[1] = {cuuint64_t(kHeadDim)};
+    const cuuint32_t box[2] = {cuuint32_t(kHeadDim), cuuint32_t(kPage)};
+    if (!encode_tensor_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.k_cache, 2, dims, strides, box) ||
+        !encode_tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.v_cache, 2, dims, strides, box))
+      return PKV_ERR_LAUNCH;
     switch (GH) {
-      case 1: return launch_decode<1, true>(ctx, dp);
-      case 2: return launch_decode<2, true>(ctx, dp);
-      default: return launch_decode<4, true>(ctx, dp);
+      case 1: return launch_decode<1, true>(ctx, dp, tk, tv);
+      case 2: return launch_decode<2, true>(ctx, dp, tk, tv);
+      default: return launch_decode<4, true>(ctx, dp, tk, tv);
     }
   }
   switch (GH) {
-    case 1: return launch_decode<1, false>(ctx, dp);
-    case 2: return launch_decode<2, false>(ctx, dp);
-    default: return launch_decode<4, false>(ctx, dp);
+    case 1: return launch_decode<1, false>(ctx, dp, tk, tv);
+    case 2: return launch_decode<2, false>(ctx, dp, tk, tv);
+    default: return launch_decode<4, false>(ctx, dp, tk, tv);
   }
 }
 

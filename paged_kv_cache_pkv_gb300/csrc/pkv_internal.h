@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/pkv.h"
@@ -88,6 +89,12 @@ int prefill_max_tiles(const pkv_desc& d, int32_t num_seqs, int32_t num_tokens);
 int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, void* scratch, int split_max_q,
                    int max_tiles);
 // Shared-prefix pass: key chunks of the prefix and tiles per chunk.
+// A tiled TMA descriptor with 128-byte swizzle (rank <= 3; strides in bytes
+// for dims 1..rank-1).  Returns false when the driver entry point is missing
+// or the driver rejects the description.
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
+                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box);
+
 int prefix_chunks(const pkv_desc& d, int32_t num_tokens, int32_t prefix_pages, int* chunk_tiles);
 // Every query row against the shared prefix pages -> partial records.
 int launch_prefix(const LaunchCtx& ctx, const AttendArgs& a, float* records, int chunks,
