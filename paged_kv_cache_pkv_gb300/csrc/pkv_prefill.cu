@@ -62,10 +62,14 @@ constexpr float kPfTau = 8.0f;
 
 // Shared-memory map (offsets from a 1024-byte aligned base); P lives in TMEM.
 constexpr uint32_t kHalfTile = 128 * 128;          // 128 rows x 64 bf16 = 16 KiB
-constexpr uint32_t kOffQ = 0;                      // [2 halves]
-constexpr uint32_t kOffK = kOffQ + 2 * kHalfTile;  // [2 bufs][2 halves]
-constexpr uint32_t kOffV = kOffK + 4 * kHalfTile;  // [2 bufs][2 halves]
-constexpr uint32_t kOffMisc = kOffV + 4 * kHalfTile;
+// K and V tiles each have kKVBufs buffers: a tile's load is issued when the
+// MMA that read the same buffer kKVBufs tiles earlier is done, which covers
+// the load latency of 8 random pages (about 1.3 us) at the tile cadence.
+constexpr int kKVBufs = 3;
+constexpr uint32_t kOffQ = 0;                                    // [2 halves]
+constexpr uint32_t kOffK = kOffQ + 2 * kHalfTile;                // [bufs][2 halves]
+constexpr uint32_t kOffV = kOffK + 2 * kKVBufs * kHalfTile;      // [bufs][2 halves]
+constexpr uint32_t kOffMisc = kOffV + 2 * kKVBufs * kHalfTile;
 constexpr uint32_t kPfMisc = 1536;  // barriers, TMEM address, tile info, scan sums, row exchange
 constexpr uint32_t kPfSmemBytes = kOffMisc + kPfMisc + 1024;  // + alignment slack
 static_assert(kPfSmemBytes <= 232448, "prefill shared memory above the 227 KiB per-CTA limit");
@@ -223,19 +227,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint8_t* sK = sm + kOffK;
   uint8_t* sV = sm + kOffV;
   // misc region: 16 barrier slots, TMEM address, tile info, row exchange
-  static_assert(11 * 8 <= 128 && 144 + 4 * (kPfThreads / 32) <= 256 && 256 + 2 * 128 * 4 <= kPfMisc,
+  constexpr int kBars = 7 + 4 * kKVBufs;
+  static_assert(kBars * 8 <= 192 && 208 + 4 * (kPfThreads / 32) <= 256 && 256 + 2 * 128 * 4 <= kPfMisc,
                 "prefill misc region layout");
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffMisc);
-  uint64_t* bar_q = bars;       // Q landed
-  uint64_t* bar_k = bars + 1;   // [2] K tile landed in buffer b
-  uint64_t* bar_v = bars + 3;   // [2] V tile landed in buffer b
-  uint64_t* bar_s = bars + 5;   // [2] S of a tile computed into TMEM buffer b
-  uint64_t* bar_o = bars + 7;   // [2] PV that read P buffer b done
-  uint64_t* bar_p = bars + 9;   // [2] P buffer b written by the softmax (256 arrivals)
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 128);  // after 16 barrier slots
-  int* s_info = reinterpret_cast<int*>(sm + kOffMisc + 136);  // b, t0
+  uint64_t* bar_q = bars;                     // Q landed
+  uint64_t* bar_s = bars + 1;                 // [2] S of a tile computed into TMEM buffer b
+  uint64_t* bar_o = bars + 3;                 // [2] PV that read P buffer b done
+  uint64_t* bar_p = bars + 5;                 // [2] P buffer b written by the softmax (256 arrivals)
+  uint64_t* bar_k = bars + 7;                 // [kKVBufs] K tile landed in buffer b
+  uint64_t* bar_v = bar_k + kKVBufs;          // [kKVBufs] V tile landed in buffer b
+  uint64_t* bar_kfree = bar_v + kKVBufs;      // [kKVBufs] the S MMA reading K buffer b is done
+  uint64_t* bar_vfree = bar_kfree + kKVBufs;  // [kKVBufs] the PV MMA reading V buffer b is done
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 192);  // after 24 barrier slots
+  int* s_info = reinterpret_cast<int*>(sm + kOffMisc + 200);  // b, t0
   int* s_scan = reinterpret_cast<int*>(sK);  // plan scratch (before any K tile lands)
-  int* s_wsum = reinterpret_cast<int*>(sm + kOffMisc + 144);  // [warps] scan sums
+  int* s_wsum = reinterpret_cast<int*>(sm + kOffMisc + 208);  // [warps] scan sums
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = blockIdx.x;  // kv head; blockIdx.y = tile (real tiles dispatch first)
@@ -323,7 +330,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   // ---- barriers and TMEM -----------------------------------------------------
   if (tid == 0) {
-    for (int i = 0; i < 9; ++i) mbar_init(bars + i, 1);
+    for (int i = 0; i < kBars; ++i) mbar_init(bars + i, 1);
     // One barrier per P buffer: the softmax can be a tile ahead of the MMA
     // lane, never two on the same buffer (it needs PV(i) before P(i+2)).
     mbar_init(bar_p, kPfSoftmaxThreads);
@@ -348,14 +355,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t idesc_o = idesc_bf16(128, 128, true);
   const int role = warp - kPfSoftmaxThreads / 32;  // 0: K loads, 1: V loads, 2: MMA; < 0 softmax
 
-  // block ids of the 8 pages of K/V tile kt (pages past the sequence: -1)
-  auto page_ids = [&](int kt, int (&bids)[kPfPagesPerTile]) {  // kt: tile of this CTA's window
-#pragma unroll
-    for (int j = 0; j < kPfPagesPerTile; ++j) {
-      const int pi = (kbeg + kt) * kPfPagesPerTile + j;
-      bids[j] = pi < npages ? __ldg(bt_row + pi) : -1;
-    }
-  };
   auto load_tile = [&](const CUtensorMap* map, uint8_t* base, uint64_t* bar, const int (&bids)[kPfPagesPerTile]) {
     int valid = 0;
 #pragma unroll
@@ -376,52 +375,72 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   };
 
   if (role == 0 || role == 1) {
-    // ===== K or V producer (one lane) =====
-    // Buffer kt&1 is free once the MMA that read tile kt-2 is done: S for K,
-    // PV for V.  Block ids of the next tile are in flight while waiting.
-    if (lane == 0) {
-      const CUtensorMap* map = role == 0 ? &tm_k : &tm_v;
-      uint8_t* base0 = role == 0 ? sK : sV;
-      uint64_t* bar_load = role == 0 ? bar_k : bar_v;
-      uint64_t* bar_free = role == 0 ? bar_s : bar_o;
-      if (role == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
-        mbar_arrive_expect_tx(bar_q, 2 * kHalfTile);
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(sQ + h * kHalfTile, &tm_q, h * 64, g * p.G, q_tok0, bar_q);
+    // ===== K or V producer (lane 0 issues; the warp fetches block ids) =====
+    // Buffer kt % kKVBufs is free once the MMA that read tile kt - kKVBufs is
+    // done (S for K, PV for V; each buffer has its own barrier, so no wait
+    // targets a phase more than one behind).  Block ids come in groups of four
+    // tiles, one page per lane, read a group ahead: a tile's copies never wait
+    // on a block-table read.
+    const CUtensorMap* map = role == 0 ? &tm_k : &tm_v;
+    uint8_t* base0 = role == 0 ? sK : sV;
+    uint64_t* bar_load = role == 0 ? bar_k : bar_v;
+    uint64_t* bar_free = role == 0 ? bar_kfree : bar_vfree;
+    if (role == 0 && lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+      mbar_arrive_expect_tx(bar_q, 2 * kHalfTile);
+      for (int h = 0; h < 2; ++h)
+        tma_load_3d(sQ + h * kHalfTile, &tm_q, h * 64, g * p.G, q_tok0, bar_q);
+    }
+    // lane l: page l % 8 of tile 4 * grp + l / 8 of this CTA's window (-1 past it)
+    auto group_id = [&](int grp) {
+      const int kt = grp * 4 + lane / kPfPagesPerTile;
+      const int pi = (kbeg + kt) * kPfPagesPerTile + lane % kPfPagesPerTile;
+      return (kt < nkv && pi < npages) ? __ldg(bt_row + pi) : -1;
+    };
+    int cur_g = group_id(0);
+    int next_g = nkv > 4 ? group_id(1) : -1;
+    int loaded = 0;
+    bool ok = true;
+    for (int kt = 0; kt < nkv; ++kt) {
+      if (kt > 0 && (kt & 3) == 0) {
+        cur_g = next_g;  // read four tiles ago
+        next_g = kt + 4 < nkv ? group_id(kt / 4 + 1) : -1;
       }
-      int ids[kPfPagesPerTile], next[kPfPagesPerTile];
-      page_ids(0, ids);
-      int loaded = 0;
-      bool ok = true;
-      for (int kt = 0; kt < nkv; ++kt) {
-        if (kt + 1 < nkv) page_ids(kt + 1, next);
-        if (kt >= 2 && !(ok = mbar_wait(bar_free + (kt & 1), ((kt - 2) >> 1) & 1))) break;
-        load_tile(map, base0 + (kt & 1) * 2 * kHalfTile, bar_load + (kt & 1), ids);
-        ++loaded;
+      int ids[kPfPagesPerTile];
 #pragma unroll
-        for (int j = 0; j < kPfPagesPerTile; ++j) ids[j] = next[j];
+      for (int j = 0; j < kPfPagesPerTile; ++j) ids[j] = __shfl_sync(0xffffffffu, cur_g, (kt & 3) * 8 + j);
+      const int kb = kt % kKVBufs;
+      if (lane == 0 && kt >= kKVBufs) ok = mbar_wait(bar_free + kb, ((kt / kKVBufs) - 1) & 1);
+      if (!__shfl_sync(0xffffffffu, int(ok), 0)) {
+        ok = false;
+        break;
       }
+      if (lane == 0) load_tile(map, base0 + kb * 2 * kHalfTile, bar_load + kb, ids);
+      ++loaded;
+    }
+    if (lane == 0) {
       // copies land before the CTA's shared memory is released
-      for (int k = max(0, loaded - 2); k < loaded; ++k)
-        mbar_wait(bar_load + (k & 1), (k >> 1) & 1, ok ? kWaitLimitNs : kDrainLimitNs);
+      for (int k = max(0, loaded - kKVBufs); k < loaded; ++k)
+        mbar_wait(bar_load + k % kKVBufs, (k / kKVBufs) & 1, ok ? kWaitLimitNs : kDrainLimitNs);
       if (!ok) flag_status(p.status, PKV_STATUS_TIMEOUT);
     }
     __syncwarp();
   } else if (role == 2) {
     // ===== MMA issuer (one lane) =====
     if (lane == 0) {
+      // S(kt): K buffer kt % kKVBufs -> TMEM S buffer kt & 1
       auto issue_s = [&](int kt) {
-        const int buf = kt & 1;
+        const int buf = kt & 1, kb = kt % kKVBufs;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const int h = ks >> 2, kk = ks & 3;
           const uint64_t a = smem_desc(smem_u32(sQ + h * kHalfTile) + kk * 32, 16, 1024);
-          const uint64_t bdesc = smem_desc(smem_u32(sK + (buf * 2 + h) * kHalfTile) + kk * 32, 16, 1024);
+          const uint64_t bdesc = smem_desc(smem_u32(sK + (kb * 2 + h) * kHalfTile) + kk * 32, 16, 1024);
           umma(tmem_s(buf), a, bdesc, idesc_s, ks > 0);
         }
         umma_commit(bar_s + buf);
+        umma_commit(bar_kfree + kb);
       };
       int ns = 0, npv = 0;
       bool ok = mbar_wait(bar_q, 0);
@@ -430,19 +449,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         issue_s(ns);
       }
       for (int it = 0; ok && it < nkv; ++it) {
-        const int buf = it & 1, ph = (it >> 1) & 1;
+        const int buf = it & 1, ph = (it >> 1) & 1, vb = it % kKVBufs;
         // P(it) written by the softmax (which also released S buffer buf); V(it) landed
-        if (!(ok = mbar_wait(bar_p + buf, ph) && mbar_wait(bar_v + buf, ph))) break;
+        if (!(ok = mbar_wait(bar_p + buf, ph) && mbar_wait(bar_v + vb, (it / kKVBufs) & 1))) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {  // 16 keys = 8 packed TMEM columns of P
-          const uint64_t bdesc = smem_desc(smem_u32(sV + buf * 2 * kHalfTile) + ks * 2048, kHalfTile, 1024);
+          const uint64_t bdesc = smem_desc(smem_u32(sV + vb * 2 * kHalfTile) + ks * 2048, kHalfTile, 1024);
           umma_ts(tmem_o, tmem_p(buf) + ks * 8, bdesc, idesc_o, (it > 0 || ks > 0) ? 1u : 0u);
         }
         umma_commit(bar_o + buf);
+        umma_commit(bar_vfree + vb);
         ++npv;
         if (ns < nkv) {  // ns == it + 2
-          if (!(ok = mbar_wait(bar_k + buf, (ns >> 1) & 1))) break;
+          if (!(ok = mbar_wait(bar_k + ns % kKVBufs, (ns / kKVBufs) & 1))) break;
           issue_s(ns++);
         }
       }
@@ -568,9 +588,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // keys past the sequence end: zero their V rows (after V landed) so
       // stale pool contents cannot leak through P = 0
       if ((kbeg + it + 1) * kPfKeys > key_end) {
-        ok = mbar_wait(bar_v + buf, ph) && ok;
+        const int vb = it % kKVBufs;
+        ok = mbar_wait(bar_v + vb, (it / kKVBufs) & 1) && ok;
         if ((kbeg + it) * kPfKeys + r >= key_end) {
-          uint4* vrow = reinterpret_cast<uint4*>(sV + (buf * 2 + ch) * kHalfTile + r * 128);
+          uint4* vrow = reinterpret_cast<uint4*>(sV + (vb * 2 + ch) * kHalfTile + r * 128);
 #pragma unroll
           for (int q = 0; q < 8; ++q) vrow[q] = make_uint4(0, 0, 0, 0);
         }
