@@ -254,8 +254,9 @@ def main():
         kc, vc = b.k_cache, b.v_cache
     out = torch.empty_like(b.q)
     desc = pkv.make_desc(kc, b.num_q_heads, bt.shape[1])
-    ws = torch.empty(pkv.workspace_size(desc, b.B, b.T, dev, int(b.info.get("shared_prefix_pages", 0))),
-                     dtype=torch.uint8, device=dev)
+    ws_bytes = (pkv.workspace_size_fp8(desc, b.B, b.T, dev) if fp8 else
+                pkv.workspace_size(desc, b.B, b.T, dev, int(b.info.get("shared_prefix_pages", 0))))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     # L2 flush before every step: write 256 MiB, then read another 256 MiB, so
     # that L2 holds neither the step's inputs nor dirty lines whose write-back
     # would otherwise land inside the next step's timed region.

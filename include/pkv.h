@@ -235,11 +235,16 @@ PKV_API int pkv_write_fp8(const pkv_bf16* k_new, const pkv_bf16* v_new,
                           pkv_fp8* k_cache, pkv_fp8* v_cache, uint8_t* k_scale,
                           uint8_t* v_scale, const pkv_desc* desc, pkv_stream_t stream);
 
+/* Workspace bytes pkv_attend_fp8 needs on the CURRENT device (its kernel
+ * runs a different number of warps than pkv_attend's).  Writes *bytes. */
+PKV_API int pkv_attend_fp8_workspace_size(const pkv_desc* desc, int32_t num_seqs,
+                                          int32_t num_tokens, size_t* bytes);
+
 /* pkv_attend_fp8 -- pkv_attend over FP8 pages: the same result with K and V
  * the exact values code * 2^(scale - 127).  Every query row runs on the
  * split-KV kernel (no tensor-core prefill and no shared-prefix cascade for
- * FP8 pages).  workspace: at least pkv_attend_workspace_size(desc, num_seqs,
- * num_tokens, 0) bytes.  Scale bytes of rows a query sees must lie in
+ * FP8 pages).  workspace: at least pkv_attend_fp8_workspace_size(desc,
+ * num_seqs, num_tokens) bytes, 256-byte aligned, no initialisation needed.  Scale bytes of rows a query sees must lie in
  * [1, 254] (pkv_write_fp8 writes nothing else); rows it does not see are
  * never used, whatever they hold. */
 PKV_API int pkv_attend_fp8(const pkv_bf16* q, const pkv_fp8* k_cache,

@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "PkvError", "PkvUnavailable", "lib", "library_path", "Desc", "write", "attend",
     "workspace_size", "get_last_error", "launch_count", "Trace", "PagePool", "KERNELS",
-    "export_pages", "import_pages", "write_fp8", "attend_fp8",
+    "export_pages", "import_pages", "write_fp8", "attend_fp8", "workspace_size_fp8",
     "STATUS_BAD_SLOT", "STATUS_BAD_BLOCK", "STATUS_BAD_QUERY", "STATUS_TIMEOUT",
 ]
 
@@ -57,6 +57,7 @@ _SIGS = {
     "pkv_attend_static": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                          ctypes.c_float, _vp, ctypes.POINTER(Desc), _vp]),
     "pkv_write_fp8": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, ctypes.POINTER(Desc), _vp]),
+    "pkv_attend_fp8_workspace_size": (ctypes.c_int, [ctypes.POINTER(Desc), _i32, _i32, ctypes.POINTER(_sz)]),
     "pkv_attend_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float,
                                       _vp, _vp, _sz, ctypes.POINTER(Desc), _vp]),
     "pkv_get_last_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
@@ -235,6 +236,15 @@ def write_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, st
                "pkv_write_fp8")
 
 
+def workspace_size_fp8(desc, num_seqs, num_tokens, device=None):
+    """Workspace bytes attend_fp8 needs for a batch of this size."""
+    n = _sz(0)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        _check(lib().pkv_attend_fp8_workspace_size(ctypes.byref(desc), int(num_seqs), int(num_tokens),
+                                                   ctypes.byref(n)), "pkv_attend_fp8_workspace_size")
+    return n.value
+
+
 def attend_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, query_start_loc, scale,
                out=None, workspace=None, stream=None):
     """attend() over FP8 pages (codes and per-row scale bytes as written by
@@ -257,7 +267,7 @@ def attend_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, qu
         _need(out, "out", torch.bfloat16, 3)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
-    need = workspace_size(desc, B, T, q.device, 0)
+    need = workspace_size_fp8(desc, B, T, q.device)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     else:

@@ -75,10 +75,7 @@ const DeviceInfo* current_device(int* err) {
   // the head ratios that need it instead of failing here.
   for (int v = 0; v < 3; ++v) {
     fresh.dec_warps[v] = fresh.sm_count * decode_ctas_per_sm(v, false) * kDecWarps;
-    // the FP8 variant shares the bf16 workspace layout, so it never runs on
-    // more warps than the bf16 one
-    fresh.dec_warps_f8[v] =
-        std::min(fresh.dec_warps[v], fresh.sm_count * decode_ctas_per_sm(v, true) * kDecWarps);
+    fresh.dec_warps_f8[v] = fresh.sm_count * decode_ctas_per_sm(v, true) * kDecWarpsF8;
   }
   void* addr = nullptr;
   if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) {
@@ -174,6 +171,18 @@ int pkv_attend_workspace_size(const pkv_desc* desc, int32_t num_seqs, int32_t nu
   const DeviceInfo* dev = current_device(&err);
   if (!dev) return err;
   *bytes = attend_workspace_bytes(*dev, *desc, num_seqs, num_tokens, shared_prefix_pages);
+  return PKV_OK;
+}
+
+int pkv_attend_fp8_workspace_size(const pkv_desc* desc, int32_t num_seqs, int32_t num_tokens,
+                                  size_t* bytes) {
+  if (int e = check_desc(desc)) return e;
+  if (!bytes) return PKV_ERR_NULL;
+  if (num_seqs < 0 || num_tokens < 0) return PKV_ERR_RANGE;
+  int err = PKV_OK;
+  const DeviceInfo* dev = current_device(&err);
+  if (!dev) return err;
+  *bytes = attend_workspace_bytes(*dev, *desc, num_seqs, num_tokens, 0, true);
   return PKV_OK;
 }
 

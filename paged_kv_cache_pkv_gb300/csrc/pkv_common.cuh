@@ -30,10 +30,15 @@ constexpr int kScaleBytes = kPage;                // FP8 row scales of one (page
 constexpr int kDecWarps = PKV_DEC_WARPS;    // warps per CTA
 constexpr int kDecStages = PKV_DEC_STAGES;  // pages (K+V) in flight per warp
 #ifndef PKV_DEC_STAGES_F8
-#define PKV_DEC_STAGES_F8 5
+#define PKV_DEC_STAGES_F8 3
 #endif
-// FP8 pages are half the bytes, so a warp keeps more of them in flight
+#ifndef PKV_DEC_WARPS_F8
+#define PKV_DEC_WARPS_F8 12
+#endif
+// The FP8 variant is bound by instruction latency, not bytes in flight: it
+// runs more warps per SM (at most 168 registers each) with 3-stage rings.
 constexpr int kDecStagesF8 = PKV_DEC_STAGES_F8;
+constexpr int kDecWarpsF8 = PKV_DEC_WARPS_F8;
 constexpr int kMaxGroupPerItem = 4;  // query heads sharing one page read
 
 // A decode partial state of one warp: m[4], l[4], then o[heads][128] (fp32).

@@ -371,7 +371,7 @@ __device__ __forceinline__ void merge_item(const DecodeParams& p, int lane, int 
 // tmk / tmv: TMA descriptors of the FP8 pools viewed as [rows][128 codes]
 // (unused by the bf16 variant).
 template <int GH, bool F8>
-__global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS)
+__global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_MIN_CTAS)
     pkv_decode_kernel(DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -379,16 +379,18 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS)
   const int wib = threadIdx.x >> 5;
   using Ring = DecRing<F8>;
   constexpr int NS = F8 ? kDecStagesF8 : kDecStages;  // ring stages
+  constexpr int NW = F8 ? kDecWarpsF8 : kDecWarps;    // warps per CTA
+  constexpr int NT = NW * 32;
   // the swizzled FP8 pages need 1024-byte aligned stages
   uint8_t* smem = F8 ? reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                   ~uintptr_t(1023))
                      : smem_raw;
   Ring& R = reinterpret_cast<Ring*>(smem)[wib];
-  int* s_start = reinterpret_cast<int*>(smem + sizeof(Ring) * kDecWarps);
+  int* s_start = reinterpret_cast<int*>(smem + sizeof(Ring) * NW);
   int* s_q0 = s_start + (p.B + 1);
   int* s_len = s_q0 + (p.B + 1);
   const SeqSmem sq{s_start, s_q0, s_len};
-  __shared__ int s_wsum[kDecWarps];
+  __shared__ int s_wsum[NW];
 
   if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(&R.bar[s], 1);
@@ -403,7 +405,7 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS)
   const int per_row = p.Hkv * p.nsub;
   {
     const int tid = threadIdx.x;
-    const int per = (p.B + kDecThreads - 1) / kDecThreads;
+    const int per = (p.B + NT - 1) / NT;
     const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
     int local = 0;
     for (int b = b0; b < b1; ++b) {
@@ -437,7 +439,7 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS)
     __syncthreads();
     int base = 0, total = 0;
 #pragma unroll
-    for (int x = 0; x < kDecWarps; ++x) {
+    for (int x = 0; x < NW; ++x) {
       if (x < wib) base += s_wsum[x];
       total += s_wsum[x];
     }
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(kDecThreads, PKV_DEC_MIN_CTAS)
   // equal contiguous ranges, at least kMinChunk pages so small batches do not
   // shatter into one-page partials
   const int chunk = max(kMinChunk, (U + p.nwarps - 1) / p.nwarps);
-  const int w = blockIdx.x * kDecWarps + wib;
+  const int w = blockIdx.x * NW + wib;
   if (w >= p.nwarps || int64_t(w) * chunk >= U) return;
   const int u_begin = w * chunk;
   const int n_units = min(U - u_begin, chunk);
@@ -1164,7 +1166,8 @@ static int variant_of(int gh) { return gh == 4 ? 2 : gh - 1; }
 // ([B+1] each) and seq_lens ([B]).
 template <bool F8>
 static size_t decode_smem_bytes(int num_seqs) {
-  return (F8 ? 1024 : 0) + sizeof(DecRing<F8>) * kDecWarps + sizeof(int) * (3 * size_t(num_seqs) + 2);
+  return (F8 ? 1024 : 0) + sizeof(DecRing<F8>) * (F8 ? kDecWarpsF8 : kDecWarps) +
+         sizeof(int) * (3 * size_t(num_seqs) + 2);
 }
 
 template <int GH, bool F8>
@@ -1176,7 +1179,8 @@ static int occupancy_for() {
     return 0;
   }
   int blocks = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, kDecThreads, smem) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, (F8 ? kDecWarpsF8 : kDecWarps) * 32, smem) !=
+      cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -1219,10 +1223,11 @@ static size_t prefix_records(const pkv_desc& d, int32_t num_tokens, int32_t pref
 }
 
 size_t attend_workspace_bytes(const DeviceInfo& dev, const pkv_desc& d, int32_t num_seqs,
-                              int32_t num_tokens, int32_t shared_prefix_pages) {
+                              int32_t num_tokens, int32_t shared_prefix_pages, bool fp8) {
   const int G = d.num_q_heads / d.num_kv_heads;
   const int gh = group_per_item(G);
-  return workspace_layout(num_tokens, d.num_kv_heads * (G / gh), dev.dec_warps[variant_of(gh)], gh,
+  const int nw = fp8 ? dev.dec_warps_f8[variant_of(gh)] : dev.dec_warps[variant_of(gh)];
+  return workspace_layout(num_tokens, d.num_kv_heads * (G / gh), nw, gh,
                           prefill_max_tiles(d, num_seqs, num_tokens),
                           prefix_records(d, num_tokens, shared_prefix_pages))
       .total;
@@ -1232,8 +1237,9 @@ template <int GH, bool F8>
 static int launch_decode(const LaunchCtx& ctx, const DecodeParams& dp, const CUtensorMap& tk,
                          const CUtensorMap& tv) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(dp.nwarps / kDecWarps);
-  cfg.blockDim = dim3(kDecThreads);
+  constexpr int NW = F8 ? kDecWarpsF8 : kDecWarps;
+  cfg.gridDim = dim3(dp.nwarps / NW);
+  cfg.blockDim = dim3(NW * 32);
   cfg.dynamicSmemBytes = decode_smem_bytes<F8>(dp.B);
   cfg.stream = ctx.stream;
   cudaLaunchAttribute attr[1];
@@ -1251,8 +1257,6 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   const int G = d.num_q_heads / d.num_kv_heads;
   const int GH = group_per_item(G);
   const int nsub = G / GH;
-  // the FP8 variant runs on at most as many warps as the bf16 one, whose count
-  // sizes the workspace
   const int nwarps = a.fp8 ? ctx.dev->dec_warps_f8[variant_of(GH)] : ctx.dev->dec_warps[variant_of(GH)];
   if (nwarps <= 0) return PKV_ERR_LAUNCH;
   if (a.fp8 && a.shared_prefix_pages != 0) return PKV_ERR_RANGE;

@@ -17,7 +17,7 @@ struct DeviceInfo {
   // Decode warps of one persistent launch, per kernel variant: index 0, 1, 2
   // for 1, 2, 4 query heads sharing a page read.
   int dec_warps[3] = {0, 0, 0};
-  int dec_warps_f8[3] = {0, 0, 0};  // FP8-page variant, never above dec_warps
+  int dec_warps_f8[3] = {0, 0, 0};  // FP8-page variant (its own CTA shape)
   size_t smem_optin = 0;
 };
 
@@ -76,7 +76,7 @@ struct AttendArgs {
 
 // Workspace bytes for a batch on the current device.
 size_t attend_workspace_bytes(const DeviceInfo& dev, const pkv_desc& d, int32_t num_seqs,
-                              int32_t num_tokens, int32_t shared_prefix_pages);
+                              int32_t num_tokens, int32_t shared_prefix_pages, bool fp8 = false);
 int launch_attend(const LaunchCtx& ctx, const AttendArgs& a);
 
 // Resident CTAs per SM of the decode kernel variant (occupancy query).

@@ -203,7 +203,7 @@ def test_attend_fp8_rejects_bad_arguments(pkvlib):
     meta = to_device(b)
     lib = pkv.lib()
     desc = pkv.make_desc(kc, b.num_q_heads, b.block_tables.shape[1])
-    ws = torch.empty(pkv.workspace_size(desc, b.B, b.T, "cuda"), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(pkv.workspace_size_fp8(desc, b.B, b.T, "cuda"), dtype=torch.uint8, device="cuda")
     out = torch.empty_like(b.q)
     import ctypes
     P = pkv._ptr
@@ -213,4 +213,8 @@ def test_attend_fp8_rejects_bad_arguments(pkvlib):
     assert lib.pkv_attend_fp8(*args(ctypes.c_void_p(0))) == -1          # PKV_ERR_NULL
     assert lib.pkv_attend_fp8(*args(ctypes.c_void_p(ks.data_ptr() + 1))) == -2  # PKV_ERR_ALIGN
     assert lib.pkv_attend_fp8(*args(P(ks))) == 0
+    short = ctypes.c_size_t(ws.numel() - 256)
+    a = list(args(P(ks)))
+    a[13] = short
+    assert lib.pkv_attend_fp8(*a) == -5  # PKV_ERR_WORKSPACE
     torch.cuda.synchronize()
