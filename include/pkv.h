@@ -200,7 +200,7 @@ PKV_API int pkv_attend(const pkv_bf16* q, const pkv_bf16* k_cache,
  *     call left there; the kernels need none of it cleared first.  Calls
  *     whose work overlaps on the GPU (different streams, no ordering between
  *     them) race on the array and give undefined results: serialise them. */
-#define PKV_STATIC_SCRATCH_BYTES (8u << 20)
+#define PKV_STATIC_SCRATCH_BYTES (16u << 20)
 PKV_API int pkv_attend_static(const pkv_bf16* q, const pkv_bf16* k_cache,
                               const pkv_bf16* v_cache, const int32_t* block_tables,
                               const int32_t* seq_lens, const int32_t* query_start_loc,

@@ -19,10 +19,10 @@ constexpr int kScaleBytes = kPage;                // FP8 row scales of one (page
 
 // Split-KV decode kernel shape.
 #ifndef PKV_DEC_WARPS
-#define PKV_DEC_WARPS 8
+#define PKV_DEC_WARPS 12
 #endif
 #ifndef PKV_DEC_STAGES
-#define PKV_DEC_STAGES 3
+#define PKV_DEC_STAGES 2
 #endif
 #ifndef PKV_DEC_MIN_CTAS
 #define PKV_DEC_MIN_CTAS 1
@@ -35,8 +35,7 @@ constexpr int kDecStages = PKV_DEC_STAGES;  // pages (K+V) in flight per warp
 #ifndef PKV_DEC_WARPS_F8
 #define PKV_DEC_WARPS_F8 12
 #endif
-// The FP8 variant is bound by instruction latency, not bytes in flight: it
-// runs more warps per SM (at most 168 registers each) with 3-stage rings.
+// FP8 pages are half the bytes: the same 12 warps keep 3 of them in flight.
 constexpr int kDecStagesF8 = PKV_DEC_STAGES_F8;
 constexpr int kDecWarpsF8 = PKV_DEC_WARPS_F8;
 constexpr int kMaxGroupPerItem = 4;  // query heads sharing one page read

@@ -1,6 +1,5 @@
-// pkv_decode.cu -- split-KV paged attention on CUDA cores for decode rows,
-// with the work plan and the log-sum-exp merge of split partials fused into
-// the same kernel.
+// pkv_decode.cu -- split-KV paged attention for decode rows, with the work
+// plan and the log-sum-exp merge of split partials fused into the same kernel.
 //
 // What is computed (llm-d blog post "What does production-grade LLM inference
 // look like?", introduction: paged attention over a paged KV cache; decode is
@@ -11,44 +10,41 @@
 //
 // Design (GB300):
 //  * Work unit = one (query row, group of GH query heads sharing a kv head,
-//    page).  A unit moves exactly one 4 KiB K page and one 4 KiB V page of one
-//    kv head (pool layout [NB, Hkv, 16, 128] makes each one contiguous block);
-//    the GH query heads reuse that read (GQA).
+//    page).  A unit moves exactly one K page and one V page of one kv head
+//    (pool layout [NB, Hkv, 16, 128] makes each one contiguous block: 4 KiB
+//    in bf16, 2 KiB of FP8 codes); the GH query heads reuse that read (GQA).
 //  * Plan: every CTA reads seq_lens / query_start_loc (tiny) and builds the
 //    per-sequence unit prefix in shared memory; units are numbered row-major
 //    and each decode warp takes an equal contiguous range, so 16-token and
 //    32768-token sequences are balanced to within one page.
-//  * Each warp is an independent worker with its own 3-stage ring: lane 0
-//    issues cp.async.bulk copies (one per 4 KiB page, L2 evict-first) that
+//  * Each warp is an independent worker with its own ring (2 stages for bf16
+//    pages, 3 for FP8): lane 0 issues the copies (L2 evict-first) that
 //    complete on an mbarrier; all 32 lanes compute.  No CTA barrier sits on
 //    the page loop.
-//  * QK^T: lane (c = lane%8, g = lane/8) owns dims {8c..8c+7, 64+8c..64+8c+7}
-//    of tokens g, g+4, g+8, g+12 and uses packed fp32x2 FMAs; partial dots are
-//    reduced over the 8 lanes of a token by a transposing butterfly (each step
-//    halves the values a lane holds): 16 dot products cost 14 shuffles.
-//  * Online softmax in the log2 domain (q pre-scaled by scale*log2 e); the
+//  * Page products on warp-level MMAs (mma.sync m16n8k16, f32 accumulators)
+//    fed straight from registers: S^T[16 tokens x 8 heads] = K . Q^T, then
+//    O^T[128 dims x 8 heads] += V^T . P^T (the GH <= 4 heads of a group pad
+//    N = 8).  The contraction index of both products is permuted so that
+//    every lane's operands are whole 16-byte pieces of shared memory: lane
+//    (g, t) reads dims 32t..32t+31 of K rows g and g+8 and dims 16g..16g+15
+//    of V rows 2t, 2t+1, 2t+8, 2t+9.  A tcgen05 MMA needs M >= 64 and its
+//    operands in shared memory or TMEM; this product has M = 16 and its
+//    operands come from registers, so the warp-level MMA is the fit.  It needs
+//    about a quarter of the instructions of packed FMAs, which lets a CTA run
+//    12 warps (168 registers) and hide more latency.
+//  * bf16 pages: bf16 operands as stored (q too), P rounded to bf16; pages by
+//    cp.async.bulk.  FP8 pages (template flag F8): 2 KiB pages of E4M3 codes
+//    by TMA tensor copies with 128-byte swizzle (conflict-free fragment reads)
+//    plus 16-byte blocks of per-row scale bytes (scale = 2^(byte-127)) by bulk
+//    copies; codes are widened exactly to f16 (E4M3 is a subset of f16), q is
+//    scaled by a power of two into f16 range (exact), P is f16.  Row scales:
+//    the K one multiplies the finished score; the V one weights the
+//    probability relative to the largest V scale of the segment (a running
+//    exponent, like the softmax maximum).
+//  * Online softmax in the log2 domain (scores scaled by scale*log2 e); the
 //    running maximum only moves when a score exceeds it by more than kTau (a
-//    warp vote), so most pages skip the max reduction and the rescale.
-//  * PV: lane (dc = lane%16, parity = lane/16) owns dims 8dc..8dc+7 of
-//    even/odd tokens, packed fp32x2 FMAs; probabilities are broadcast through
-//    shared memory as (p, p) pairs.
-//  * FP8 pages (template flag F8): the unit moves a 2 KiB K page and a 2 KiB V
-//    page of E4M3 codes (TMA tensor copies with 128-byte swizzle, so the
-//    fragment reads below are bank-conflict free) plus their 16-byte blocks
-//    of per-row scale bytes (scale = 2^(byte-127)).  Widening each code costs
-//    as much as the math it feeds on CUDA cores, so the page's two small
-//    products run as mma.sync m16n8k16 (f16 in, f32 accumulate) straight
-//    from registers: S^T[16 tokens x 8 heads] = K . Q^T with the codes
-//    widened exactly to f16 (E4M3 is a subset of f16) and q scaled by a power
-//    of two into f16 range (exact), then O^T[128 dims x 8 heads] += V^T . P^T
-//    with P in f16.  The contraction index of both products is permuted so
-//    that every lane's operands are whole 16-byte rows of shared memory.
-//    Row scales: the K one multiplies the finished score; the V one weights
-//    the probability relative to the largest V scale seen in the segment
-//    (kept as a running exponent, like the softmax maximum).  A tcgen05 MMA
-//    needs M >= 64 and operands in shared memory; this product has M = 16
-//    and its operands are converted in registers, so the warp-level MMA is
-//    the fit.
+//    warp vote), so most pages skip the max reduction and the rescale.  P
+//    moves from the score fragment to the PV operand fragment with 4 shuffles.
 //  * A warp that sees a whole (row, head group) writes bf16 output directly.
 //    A split one writes (m, l, o) to one of its two partial slots and bumps
 //    an epoch-tagged arrival counter; the last warp to arrive merges the
@@ -102,8 +98,7 @@ template <bool F8>
 struct DecRing;
 template <>
 struct __align__(128) DecRing<false> {
-  uint4 kv[kDecStages][2][kPageBytes / 16];  // [stage][K|V][16 rows x 16 vec]
-  float2 ps[kPage * kMaxGroupPerItem];        // (p, p) pairs [token][head]
+  uint4 kv[kDecStages][2][kPageBytes / 16];  // [stage][K|V][16 rows x 256 B]
   StageDesc desc[kDecStages];
   uint64_t bar[kDecStages];
 };
@@ -111,7 +106,6 @@ template <>
 struct __align__(1024) DecRing<true> {
   uint8_t kv[kDecStagesF8][2][kPageBytesF8];  // 128-byte-swizzled [16 rows][128 codes]
   uint4 sc[kDecStagesF8][2];                  // K and V row scale bytes
-  float ot[kMaxGroupPerItem * kHeadDim];      // O transposed at a segment's end
   StageDesc desc[kDecStagesF8];
   uint64_t bar[kDecStagesF8];
 };
@@ -138,6 +132,16 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
                                         uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D += A . B, m16n8k16, bf16 operands, f32 accumulators (warp-collective).
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -513,28 +517,21 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
   }
 
   // ---- consumer state ----------------------------------------------------------
-  constexpr int NVL = GH == 4 ? 2 : 1;  // scores a lane holds after the butterfly
-  const int c8 = lane & 7, grp = lane >> 3;
-  const int h1 = (lane >> 2) & 1, h2 = (lane >> 1) & 1, h3 = lane & 1;
-  const int my_tok = grp + 4 * (2 * h1 + h2);
-  const int dc = lane & 15, par = lane >> 4;
-  auto head_of = [&](int k) { return GH == 4 ? 2 * h3 + k : (GH == 2 ? h3 : 0); };
-
-  float2 qf[GH][8];  // (dim 2e, 2e+1) pairs of this lane's 16 dims, pre-scaled
-  float2 o[GH][4];   // dims 8dc+2e, 8dc+2e+1
-  float m[GH];
-  float lsum[NVL];
-  // FP8 (MMA fragments): lane = (gq = lane/4, tq = lane%4).  qb: Q^T operand
-  // of head gq, dims 32tq+4s+{0,1} / {2,3} for k-step s; oacc: O^T of dims
-  // 16gq+2mb+{0,1} (M-block mb) for heads 2tq, 2tq+1; m2 / l2 the running
-  // maximum and sum of those two heads over this lane's tokens gq, gq+8.
+  // MMA fragments: lane = (gq = lane/4, tq = lane%4).  qb: Q^T operand of head
+  // gq, dims 32tq+4s+{0,1} / {2,3} for k-step s; oacc: O^T of dims
+  // 16gq+2mb+{0,1} (M-block mb) for heads 2tq, 2tq+1; m2 / l2: the running
+  // maximum (log2 domain) and sum of those two heads over this lane's tokens
+  // gq, gq+8.  At a segment's end they move to the flush layout: o by lanes
+  // (dc, par), m and l of every head on every lane.
   const int gq = lane >> 2, tq = lane & 3;
+  const int dc = lane & 15, par = lane >> 4;
   uint32_t qb[8][2];
   float oacc[8][4];
   float m2[2], l2[2];
-  float qmul = 0.f;   // scale * log2(e) * 2^-kq
-  int eref = 0;       // largest V scale byte of the segment so far (0: none)
-  float lfin[GH];     // FP8: per-head sums, ready for the flush
+  float qmul = 0.f;  // scale * log2(e) (FP8: times 2^-kq)
+  int eref = 0;      // FP8: largest V scale byte of the segment so far (0: none)
+  float2 o[GH][4];   // flush layout: dims 8dc+2e, 8dc+2e+1 of head h
+  float m[GH], lfin[GH];
   int cur_row = -1, cur_item = -1, cur_item_start = 0, cur_seg_start = 0, cur_nvis = 0, cur_h0 = 0;
 
   auto start_segment = [&](const StageDesc& d, int u) {
@@ -546,7 +543,19 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
     const int g = d.item / p.nsub, sub = d.item - g * p.nsub;
     cur_h0 = g * p.G + sub * GH;
     const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (size_t(d.row) * p.Hq + cur_h0) * kHeadDim);
-    if constexpr (F8) {
+    if constexpr (!F8) {
+      // bf16 pages: the Q^T operand is q's own bf16 pairs (zero past the group)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if (gq < GH) x = __ldg(qrow + gq * 16 + tq * 4 + c);
+        qb[2 * c][0] = x.x;
+        qb[2 * c][1] = x.y;
+        qb[2 * c + 1][0] = x.z;
+        qb[2 * c + 1][1] = x.w;
+      }
+      qmul = p.qscale;
+    } else {
       // head gq's dims 32tq..32tq+31 (zero for heads past the group)
       float qv[32];
       float amax = 0.f;
@@ -575,78 +584,50 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
         qb[st][0] = pack_f16x2(qv[4 * st] * up, qv[4 * st + 1] * up);
         qb[st][1] = pack_f16x2(qv[4 * st + 2] * up, qv[4 * st + 3] * up);
       }
-#pragma unroll
-      for (int mb = 0; mb < 8; ++mb)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) oacc[mb][e] = 0.f;
-      m2[0] = m2[1] = -INFINITY;
-      l2[0] = l2[1] = 0.f;
-      eref = 0;
-#pragma unroll
-      for (int k = 0; k < NVL; ++k) lsum[k] = 0.f;
-    } else {
-#pragma unroll
-      for (int h = 0; h < GH; ++h) {
-        // the lane's dims: {8c..8c+7, 64+8c..64+8c+7}
-        const uint4 a = __ldg(qrow + h * 16 + c8);
-        const uint4 b = __ldg(qrow + h * 16 + 8 + c8);
-        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          qf[h][e] = make_float2(bf_lo(wa[e]) * p.qscale, bf_hi(wa[e]) * p.qscale);
-          qf[h][4 + e] = make_float2(bf_lo(wb[e]) * p.qscale, bf_hi(wb[e]) * p.qscale);
-        }
-        m[h] = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[h][e] = make_float2(0.f, 0.f);
-      }
-#pragma unroll
-      for (int k = 0; k < NVL; ++k) lsum[k] = 0.f;
     }
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) oacc[mb][e] = 0.f;
+    m2[0] = m2[1] = -INFINITY;
+    l2[0] = l2[1] = 0.f;
+    eref = 0;
   };
 
-  // FP8: bring the MMA-fragment state into the layout of the split-KV path
-  // (o by (dc, par) lanes, m and l of every head on every lane).
-  auto f8_to_common = [&]() {
-    if constexpr (F8) {
-      const float os = scale_of(uint32_t(eref));
-  #pragma unroll
-      for (int mb = 0; mb < 8; ++mb) {
-        const int d0 = 16 * gq + 2 * mb;
-        if (2 * tq < GH) {
-          R.ot[(2 * tq) * kHeadDim + d0] = oacc[mb][0] * os;
-          R.ot[(2 * tq) * kHeadDim + d0 + 1] = oacc[mb][2] * os;
-        }
-        if (2 * tq + 1 < GH) {
-          R.ot[(2 * tq + 1) * kHeadDim + d0] = oacc[mb][1] * os;
-          R.ot[(2 * tq + 1) * kHeadDim + d0 + 1] = oacc[mb][3] * os;
-        }
+  // Fragment state -> flush layout.  Lane (dc, par 0) takes dims 8dc..8dc+7
+  // of head h from lane (gq = dc/2, tq = h/2), M-blocks 4(dc%2)..4(dc%2)+3;
+  // par 1 lanes hold 0.  l is summed over the lanes of a tq.
+  auto frag_to_common = [&]() {
+    const float os = F8 ? scale_of(uint32_t(eref)) : 1.f;
+#pragma unroll
+    for (int h = 0; h < GH; ++h) {
+      const int src = 4 * (dc >> 1) + (h >> 1);
+      const bool odd = dc & 1;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x0 = __shfl_sync(kFull, oacc[e][h & 1], src);
+        const float x1 = __shfl_sync(kFull, oacc[4 + e][h & 1], src);
+        const float y0 = __shfl_sync(kFull, oacc[e][2 + (h & 1)], src);
+        const float y1 = __shfl_sync(kFull, oacc[4 + e][2 + (h & 1)], src);
+        o[h][e] = par == 0 ? make_float2((odd ? x1 : x0) * os, (odd ? y1 : y0) * os) : make_float2(0.f, 0.f);
       }
-      __syncwarp();
-  #pragma unroll
-      for (int h = 0; h < GH; ++h)
-  #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          o[h][e] = par == 0 ? *reinterpret_cast<const float2*>(&R.ot[h * kHeadDim + 8 * dc + 2 * e])
-                             : make_float2(0.f, 0.f);
-      __syncwarp();
-      float lr[2] = {l2[0], l2[1]};
-  #pragma unroll
-      for (int k = 0; k < 2; ++k)
-  #pragma unroll
-        for (int o2 = 4; o2 < 32; o2 <<= 1) lr[k] += __shfl_xor_sync(kFull, lr[k], o2);
-  #pragma unroll
-      for (int h = 0; h < GH; ++h) {
-        const float mh0 = __shfl_sync(kFull, m2[0], h >> 1), mh1 = __shfl_sync(kFull, m2[1], h >> 1);
-        const float lh0 = __shfl_sync(kFull, lr[0], h >> 1), lh1 = __shfl_sync(kFull, lr[1], h >> 1);
-        m[h] = (h & 1) ? mh1 : mh0;
-        lfin[h] = (h & 1) ? lh1 : lh0;
-      }
+    }
+    float lr[2] = {l2[0], l2[1]};
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) lr[k] += __shfl_xor_sync(kFull, lr[k], o2);
+#pragma unroll
+    for (int h = 0; h < GH; ++h) {
+      const float mh0 = __shfl_sync(kFull, m2[0], h >> 1), mh1 = __shfl_sync(kFull, m2[1], h >> 1);
+      const float lh0 = __shfl_sync(kFull, lr[0], h >> 1), lh1 = __shfl_sync(kFull, lr[1], h >> 1);
+      m[h] = (h & 1) ? mh1 : mh0;
+      lfin[h] = (h & 1) ? lh1 : lh0;
     }
   };
 
   auto flush_segment = [&]() {
-    if constexpr (F8) f8_to_common();
+    frag_to_common();
 #pragma unroll
     for (int h = 0; h < GH; ++h)
 #pragma unroll
@@ -654,33 +635,9 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
         o[h][e].x += __shfl_xor_sync(kFull, o[h][e].x, 16);
         o[h][e].y += __shfl_xor_sync(kFull, o[h][e].y, 16);
       }
-    float lpart[NVL];
-#pragma unroll
-    for (int k = 0; k < NVL; ++k) {
-      float x = lsum[k];
-      x += __shfl_xor_sync(kFull, x, 2);
-      x += __shfl_xor_sync(kFull, x, 4);
-      x += __shfl_xor_sync(kFull, x, 8);
-      x += __shfl_xor_sync(kFull, x, 16);
-      lpart[k] = x;
-    }
     float l[GH];
-    if constexpr (F8) {
 #pragma unroll
-      for (int h = 0; h < GH; ++h) l[h] = lfin[h];
-    } else if constexpr (GH == 4) {
-      const float x0 = __shfl_xor_sync(kFull, lpart[0], 1), x1 = __shfl_xor_sync(kFull, lpart[1], 1);
-      l[0] = h3 ? x0 : lpart[0];
-      l[1] = h3 ? x1 : lpart[1];
-      l[2] = h3 ? lpart[0] : x0;
-      l[3] = h3 ? lpart[1] : x1;
-    } else if constexpr (GH == 2) {
-      const float x0 = __shfl_xor_sync(kFull, lpart[0], 1);
-      l[0] = h3 ? x0 : lpart[0];
-      l[1] = h3 ? lpart[0] : x0;
-    } else {
-      l[0] = lpart[0];
-    }
+    for (int h = 0; h < GH; ++h) l[h] = lfin[h];
     const int npages = (cur_nvis + kPage - 1) / kPage;
     const bool whole = cur_item_start >= u_begin && cur_item_start + npages <= u_begin + chunk;
     constexpr int HPL = GH >= 2 ? GH / 2 : 1;  // heads written per lane
@@ -970,178 +927,105 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
         mma_f16(oacc[mb], a0, a1, a2, a3, pb0, pb1);
       }
     } else {
-
-      const uint4* Ks = R.kv[stage][0];
-      const uint4* Vs = R.kv[stage][1];
-
-      // ---- V slice of this lane into registers (even/odd tokens x 8 dims) ----
-      uint4 vreg[kPage / 2];
+      // ---- bf16 pages on MMA fragments (same lane roles as FP8) ----
+      const uint8_t* Kp = reinterpret_cast<const uint8_t*>(R.kv[stage][0]);  // [16][256 B]
+      const uint8_t* Vp = reinterpret_cast<const uint8_t*>(R.kv[stage][1]);
+      // K rows gq, gq+8: dims 32tq..32tq+31 (64 bytes each)
+      uint4 ka[4], kb[4];
 #pragma unroll
-      for (int i = 0; i < kPage / 2; ++i) vreg[i] = Vs[(par + 2 * i) * 16 + dc];
-
-      // ---- scores: 4 tokens x GH heads per lane, partial over 16 dims ----
-      float v[4 * GH];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int t = grp + 4 * i;
-        const uint4 a = Ks[t * 16 + c8];
-        const uint4 b = Ks[t * 16 + 8 + c8];
-        const uint32_t wk[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        float2 kf[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) kf[e] = make_float2(bf_lo(wk[e]), bf_hi(wk[e]));
-#pragma unroll
-        for (int h = 0; h < GH; ++h) {
-          float2 acc = __fmul2_rn(qf[h][0], kf[0]);
-#pragma unroll
-          for (int e = 1; e < 8; ++e) acc = __ffma2_rn(qf[h][e], kf[e], acc);
-          v[i * GH + h] = acc.x + acc.y;
-        }
+      for (int c = 0; c < 4; ++c) {
+        ka[c] = *reinterpret_cast<const uint4*>(Kp + gq * 256 + tq * 64 + c * 16);
+        kb[c] = *reinterpret_cast<const uint4*>(Kp + (gq + 8) * 256 + tq * 64 + c * 16);
       }
-      // The page now lives in registers: hand the stage back to the copy engine.
+      // V rows 2tq, 2tq+1, 2tq+8, 2tq+9: dims 16gq..16gq+15 (32 bytes each)
+      uint4 vr[4][2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        vr[0][c] = *reinterpret_cast<const uint4*>(Vp + (2 * tq) * 256 + gq * 32 + c * 16);
+        vr[1][c] = *reinterpret_cast<const uint4*>(Vp + (2 * tq + 1) * 256 + gq * 32 + c * 16);
+        vr[2][c] = *reinterpret_cast<const uint4*>(Vp + (2 * tq + 8) * 256 + gq * 32 + c * 16);
+        vr[3][c] = *reinterpret_cast<const uint4*>(Vp + (2 * tq + 9) * 256 + gq * 32 + c * 16);
+      }
       __syncwarp();
       if (it + NS < n_units) {
         issue(stage);
         if (it + NS + 1 < n_units) cursor_advance(pc, p, sq, per_row);
       }
 
-      // transposing butterfly over lanes xor 4, 2, 1
+      // ---- S^T = K . Q^T ----
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
       {
-        constexpr int N0 = 4 * GH;
+        float sodd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < N0 / 2; ++i) {
-          const float a = v[i], b = v[i + N0 / 2];
-          const float send = h1 ? a : b, keep = h1 ? b : a;
-          v[i] = keep + __shfl_xor_sync(kFull, send, 4);
+        for (int st = 0; st < 8; ++st) {
+          const uint4& A = ka[st >> 1];
+          const uint4& B = kb[st >> 1];
+          const uint32_t a0 = (st & 1) ? A.z : A.x, a2 = (st & 1) ? A.w : A.y;
+          const uint32_t a1 = (st & 1) ? B.z : B.x, a3 = (st & 1) ? B.w : B.y;
+          mma_bf16((st & 1) ? sodd : sacc, a0, a1, a2, a3, qb[st][0], qb[st][1]);
         }
-        constexpr int N1 = N0 / 2;
 #pragma unroll
-        for (int i = 0; i < N1 / 2; ++i) {
-          const float a = v[i], b = v[i + N1 / 2];
-          const float send = h2 ? a : b, keep = h2 ? b : a;
-          v[i] = keep + __shfl_xor_sync(kFull, send, 2);
-        }
-        constexpr int N2 = N1 / 2;
-        if constexpr (N2 >= 2) {
-#pragma unroll
-          for (int i = 0; i < N2 / 2; ++i) {
-            const float a = v[i], b = v[i + N2 / 2];
-            const float send = h3 ? a : b, keep = h3 ? b : a;
-            v[i] = keep + __shfl_xor_sync(kFull, send, 1);
-          }
-        } else {
-          v[0] += __shfl_xor_sync(kFull, v[0], 1);
-        }
+        for (int e = 0; e < 4; ++e) sacc[e] += sodd[e];
       }
-      float s[NVL];
-#pragma unroll
-      for (int k = 0; k < NVL; ++k) s[k] = my_tok < nvalid ? v[k] : -INFINITY;
-
-      // ---- online softmax (log2 domain) ----
-      float mine[NVL];
-#pragma unroll
-      for (int k = 0; k < NVL; ++k) {
-        float mm = m[0];
-#pragma unroll
-        for (int x = 0; x < GH; ++x)
-          if (x == head_of(k)) mm = m[x];
-        mine[k] = mm;
-      }
-      bool exceed = false;
-#pragma unroll
-      for (int k = 0; k < NVL; ++k) exceed |= s[k] > mine[k] + kTau;
+      const bool t0 = gq < nvalid, t1 = gq + 8 < nvalid;
+      const bool h0 = 2 * tq < GH, h1r = 2 * tq + 1 < GH;
+      float sv[4];
+      sv[0] = t0 && h0 ? sacc[0] * qmul : -INFINITY;
+      sv[1] = t0 && h1r ? sacc[1] * qmul : -INFINITY;
+      sv[2] = t1 && h0 ? sacc[2] * qmul : -INFINITY;
+      sv[3] = t1 && h1r ? sacc[3] * qmul : -INFINITY;
+      const bool exceed = sv[0] > m2[0] + kTau || sv[2] > m2[0] + kTau || sv[1] > m2[1] + kTau ||
+                          sv[3] > m2[1] + kTau;
       if (__any_sync(kFull, exceed)) {
-        float pm[NVL];
+        float full0 = fmaxf(sv[0], sv[2]), full1 = fmaxf(sv[1], sv[3]);
 #pragma unroll
-        for (int k = 0; k < NVL; ++k) {
-          float x = s[k];
-          x = fmaxf(x, __shfl_xor_sync(kFull, x, 2));
-          x = fmaxf(x, __shfl_xor_sync(kFull, x, 4));
-          x = fmaxf(x, __shfl_xor_sync(kFull, x, 8));
-          x = fmaxf(x, __shfl_xor_sync(kFull, x, 16));
-          pm[k] = x;
+        for (int o2 = 4; o2 < 32; o2 <<= 1) {
+          full0 = fmaxf(full0, __shfl_xor_sync(kFull, full0, o2));
+          full1 = fmaxf(full1, __shfl_xor_sync(kFull, full1, o2));
         }
-        float full[GH];
-        if constexpr (GH == 4) {
-          const float x0 = __shfl_xor_sync(kFull, pm[0], 1), x1 = __shfl_xor_sync(kFull, pm[1], 1);
-          full[0] = h3 ? x0 : pm[0];
-          full[1] = h3 ? x1 : pm[1];
-          full[2] = h3 ? pm[0] : x0;
-          full[3] = h3 ? pm[1] : x1;
-        } else if constexpr (GH == 2) {
-          const float x0 = __shfl_xor_sync(kFull, pm[0], 1);
-          full[0] = h3 ? x0 : pm[0];
-          full[1] = h3 ? pm[0] : x0;
-        } else {
-          full[0] = pm[0];
-        }
-        float alpha[GH];
+        const float mn0 = fmaxf(m2[0], full0), mn1 = fmaxf(m2[1], full1);
+        const float a0 = m2[0] == -INFINITY ? 0.f : ex2(m2[0] - mn0);
+        const float a1 = m2[1] == -INFINITY ? 0.f : ex2(m2[1] - mn1);
+        m2[0] = mn0;
+        m2[1] = mn1;
+        l2[0] *= a0;
+        l2[1] *= a1;
 #pragma unroll
-        for (int h = 0; h < GH; ++h) {
-          const float mn = fmaxf(m[h], full[h]);
-          alpha[h] = m[h] == -INFINITY ? 0.f : ex2(m[h] - mn);
-          m[h] = mn;
-          const float2 a2 = make_float2(alpha[h], alpha[h]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o[h][e] = __fmul2_rn(o[h][e], a2);
-        }
-#pragma unroll
-        for (int k = 0; k < NVL; ++k) {
-          float a = alpha[0], mm = m[0];
-#pragma unroll
-          for (int x = 0; x < GH; ++x)
-            if (x == head_of(k)) {
-              a = alpha[x];
-              mm = m[x];
-            }
-          lsum[k] *= a;
-          mine[k] = mm;
+        for (int mb = 0; mb < 8; ++mb) {
+          oacc[mb][0] *= a0;
+          oacc[mb][1] *= a1;
+          oacc[mb][2] *= a0;
+          oacc[mb][3] *= a1;
         }
       }
-      float pr[NVL];
-#pragma unroll
-      for (int k = 0; k < NVL; ++k) {
-        pr[k] = ex2(s[k] - mine[k]);
-        lsum[k] += pr[k];
-      }
-      if constexpr (GH == 4) {
-        *reinterpret_cast<float4*>(&R.ps[my_tok * 4 + 2 * h3]) = make_float4(pr[0], pr[0], pr[1], pr[1]);
-      } else if constexpr (GH == 2) {
-        R.ps[my_tok * 2 + h3] = make_float2(pr[0], pr[0]);
-      } else {
-        R.ps[my_tok] = make_float2(pr[0], pr[0]);
-      }
-      __syncwarp();
+      const float r0 = m2[0] == -INFINITY ? 0.f : m2[0], r1 = m2[1] == -INFINITY ? 0.f : m2[1];
+      const float p0 = ex2(sv[0] - r0), p1 = ex2(sv[1] - r1), p2 = ex2(sv[2] - r0), p3 = ex2(sv[3] - r1);
+      l2[0] += p0 + p2;
+      l2[1] += p1 + p3;
+      const uint32_t pe = pack_bf16x2(p0, p2), po = pack_bf16x2(p1, p3);
+      const int src0 = 8 * tq + (gq >> 1), src1 = src0 + 4;
+      const uint32_t x0 = __shfl_sync(kFull, pe, src0), x1 = __shfl_sync(kFull, po, src0);
+      const uint32_t y0 = __shfl_sync(kFull, pe, src1), y1 = __shfl_sync(kFull, po, src1);
+      const uint32_t X = (gq & 1) ? x1 : x0, Y = (gq & 1) ? y1 : y0;
+      uint32_t pb0 = __byte_perm(X, Y, 0x5410), pb1 = __byte_perm(X, Y, 0x7632);
+      if (gq >= GH) pb0 = pb1 = 0u;
 
-      // ---- PV from registers: even/odd tokens x 8 dims per lane ----
+      // ---- O^T += V^T . P^T (rows past the sequence may hold anything) ----
+      if (nvalid < kPage) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        if (2 * tq >= nvalid) vr[0][0] = vr[0][1] = z;
+        if (2 * tq + 1 >= nvalid) vr[1][0] = vr[1][1] = z;
+        if (2 * tq + 8 >= nvalid) vr[2][0] = vr[2][1] = z;
+        if (2 * tq + 9 >= nvalid) vr[3][0] = vr[3][1] = z;
+      }
 #pragma unroll
-      for (int i = 0; i < kPage / 2; ++i) {
-        const int t = par + 2 * i;
-        if (nvalid == kPage || t < nvalid) {
-          const uint32_t wv[4] = {vreg[i].x, vreg[i].y, vreg[i].z, vreg[i].w};
-          float2 vf[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) vf[e] = make_float2(bf_lo(wv[e]), bf_hi(wv[e]));
-          float2 pv[GH];
-          if constexpr (GH == 4) {
-            const float4 x = *reinterpret_cast<const float4*>(&R.ps[t * 4]);
-            const float4 y = *reinterpret_cast<const float4*>(&R.ps[t * 4 + 2]);
-            pv[0] = make_float2(x.x, x.y);
-            pv[1] = make_float2(x.z, x.w);
-            pv[2] = make_float2(y.x, y.y);
-            pv[3] = make_float2(y.z, y.w);
-          } else if constexpr (GH == 2) {
-            const float4 x = *reinterpret_cast<const float4*>(&R.ps[t * 2]);
-            pv[0] = make_float2(x.x, x.y);
-            pv[1] = make_float2(x.z, x.w);
-          } else {
-            pv[0] = R.ps[t];
-          }
-#pragma unroll
-          for (int h = 0; h < GH; ++h)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o[h][e] = __ffma2_rn(pv[h], vf[e], o[h][e]);
-        }
+      for (int mb = 0; mb < 8; ++mb) {
+        // word mb of the 32 bytes of each row: dims 16gq+2mb, +1
+        const int k = mb & 3, hv = mb >> 2;
+        auto word = [&](const uint4& x) { return k == 0 ? x.x : (k == 1 ? x.y : (k == 2 ? x.z : x.w)); };
+        const uint32_t A = word(vr[0][hv]), B = word(vr[1][hv]), Cw = word(vr[2][hv]), Dw = word(vr[3][hv]);
+        mma_bf16(oacc[mb], __byte_perm(A, B, 0x5410), __byte_perm(A, B, 0x7632), __byte_perm(Cw, Dw, 0x5410),
+                 __byte_perm(Cw, Dw, 0x7632), pb0, pb1);
       }
     }
   }
