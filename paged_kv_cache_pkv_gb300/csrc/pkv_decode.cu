@@ -93,21 +93,21 @@ struct StageDesc {
 template <bool F8>
 constexpr int kPageBytesOf = F8 ? kPageBytesF8 : kPageBytes;
 
-// One warp's page ring.
+// One warp's page ring: K and V pages of each stage, copied by TMA with
+// 128-byte swizzle (stages 1024-byte aligned).  A bf16 page is 32 units of
+// 128 bytes (token row r = units 2r, 2r+1), an FP8 page 16 units (one per row).
 template <bool F8>
-struct DecRing;
-template <>
-struct __align__(128) DecRing<false> {
-  uint4 kv[kDecStages][2][kPageBytes / 16];  // [stage][K|V][16 rows x 256 B]
-  StageDesc desc[kDecStages];
-  uint64_t bar[kDecStages];
+struct DecRing {
+  uint8_t kv[F8 ? kDecStagesF8 : kDecStages][2][F8 ? kPageBytesF8 : kPageBytes];
 };
-template <>
-struct __align__(1024) DecRing<true> {
-  uint8_t kv[kDecStagesF8][2][kPageBytesF8];  // 128-byte-swizzled [16 rows][128 codes]
-  uint4 sc[kDecStagesF8][2];                  // K and V row scale bytes
-  StageDesc desc[kDecStagesF8];
-  uint64_t bar[kDecStagesF8];
+static_assert(sizeof(DecRing<false>) % 1024 == 0 && sizeof(DecRing<true>) % 1024 == 0,
+              "ring stages stay 1024-byte aligned");
+// Per-warp ring bookkeeping, kept apart from the aligned pages.
+template <bool F8>
+struct DecMeta {
+  uint4 sc[F8 ? kDecStagesF8 : 1][2];  // FP8: K and V row scale bytes of a stage
+  StageDesc desc[F8 ? kDecStagesF8 : kDecStages];
+  uint64_t bar[F8 ? kDecStagesF8 : kDecStages];
 };
 
 // 2^(byte - 127) for a scale byte in [1, 254]; 0 for byte 0.
@@ -154,9 +154,9 @@ __device__ __forceinline__ void bytes_t_t8(const uint4& v, int t, uint32_t& b0, 
   b1 = (((t & 4) ? v.w : v.z) >> sh) & 0xFFu;
 }
 
-// 16-byte chunk c of row r of a page copied with 128-byte swizzle.
-__device__ __forceinline__ const uint4& swz(const uint8_t* page, int r, int c) {
-  return *reinterpret_cast<const uint4*>(page + r * 128 + ((c ^ (r & 7)) << 4));
+// 16-byte chunk c of 128-byte unit u of a page copied with 128-byte swizzle.
+__device__ __forceinline__ const uint4& swz(const uint8_t* page, int u, int c) {
+  return *reinterpret_cast<const uint4*>(page + u * 128 + ((c ^ (u & 7)) << 4));
 }
 
 // 2D TMA tile load with an L2 cache hint.
@@ -382,22 +382,22 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
   using Ring = DecRing<F8>;
+  using Meta = DecMeta<F8>;
   constexpr int NS = F8 ? kDecStagesF8 : kDecStages;  // ring stages
   constexpr int NW = F8 ? kDecWarpsF8 : kDecWarps;    // warps per CTA
   constexpr int NT = NW * 32;
-  // the swizzled FP8 pages need 1024-byte aligned stages
-  uint8_t* smem = F8 ? reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                  ~uintptr_t(1023))
-                     : smem_raw;
+  // swizzled pages need 1024-byte aligned stages
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ring& R = reinterpret_cast<Ring*>(smem)[wib];
-  int* s_start = reinterpret_cast<int*>(smem + sizeof(Ring) * NW);
+  Meta& M = reinterpret_cast<Meta*>(smem + sizeof(Ring) * NW)[wib];
+  int* s_start = reinterpret_cast<int*>(smem + (sizeof(Ring) + sizeof(Meta)) * NW);
   int* s_q0 = s_start + (p.B + 1);
   int* s_len = s_q0 + (p.B + 1);
   const SeqSmem sq{s_start, s_q0, s_len};
   __shared__ int s_wsum[NW];
 
   if (lane == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(&R.bar[s], 1);
+    for (int s = 0; s < NS; ++s) mbar_init(&M.bar[s], 1);
     fence_mbar_init();
   }
   // Under programmatic dependent launch everything up to griddep_wait() below
@@ -493,17 +493,16 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
       constexpr int PB = kPageBytesOf<F8>;
       const int g = pc.item / p.nsub;
       const size_t ph = size_t(pc.bid) * p.Hkv + g;  // (page, kv head)
-      R.desc[stage] = StageDesc{pc.q0 + pc.j, pc.item, pc.item_start, pc.nvis - p.np * kPage};
-      mbar_arrive_expect_tx(&R.bar[stage], 2 * PB + (F8 ? 2 * kScaleBytes : 0));
+      M.desc[stage] = StageDesc{pc.q0 + pc.j, pc.item, pc.item_start, pc.nvis - p.np * kPage};
+      mbar_arrive_expect_tx(&M.bar[stage], 2 * PB + (F8 ? 2 * kScaleBytes : 0));
+      // one box per page: the pool viewed as [units][128 bytes]; the host
+      // checks that unit indices fit int32
+      const int unit0 = int(ph) * (PB / 128);
+      tma_load_2d_hint(&R.kv[stage][0][0], &tmk, 0, unit0, &M.bar[stage], policy);
+      tma_load_2d_hint(&R.kv[stage][1][0], &tmv, 0, unit0, &M.bar[stage], policy);
       if constexpr (F8) {
-        const int row0 = int(ph) * kPage;  // the host checks that rows fit int32
-        tma_load_2d_hint(&R.kv[stage][0][0], &tmk, 0, row0, &R.bar[stage], policy);
-        tma_load_2d_hint(&R.kv[stage][1][0], &tmv, 0, row0, &R.bar[stage], policy);
-        bulk_g2s(&R.sc[stage][0], p.k_scale + ph * kScaleBytes, kScaleBytes, &R.bar[stage], policy);
-        bulk_g2s(&R.sc[stage][1], p.v_scale + ph * kScaleBytes, kScaleBytes, &R.bar[stage], policy);
-      } else {
-        bulk_g2s(&R.kv[stage][0][0], p.k_cache + ph * PB, PB, &R.bar[stage], policy);
-        bulk_g2s(&R.kv[stage][1][0], p.v_cache + ph * PB, PB, &R.bar[stage], policy);
+        bulk_g2s(&M.sc[stage][0], p.k_scale + ph * kScaleBytes, kScaleBytes, &M.bar[stage], policy);
+        bulk_g2s(&M.sc[stage][1], p.v_scale + ph * kScaleBytes, kScaleBytes, &M.bar[stage], policy);
       }
     }
   };
@@ -595,14 +594,16 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
   };
 
   // Fragment state -> flush layout.  Lane (dc, par 0) takes dims 8dc..8dc+7
-  // of head h from lane (gq = dc/2, tq = h/2), M-blocks 4(dc%2)..4(dc%2)+3;
-  // par 1 lanes hold 0.  l is summed over the lanes of a tq.
+  // of head h from the lane with tq = h/2 that holds them; par 1 lanes hold 0.
+  // l is summed over the lanes of a tq.
   auto frag_to_common = [&]() {
     const float os = F8 ? scale_of(uint32_t(eref)) : 1.f;
 #pragma unroll
     for (int h = 0; h < GH; ++h) {
-      const int src = 4 * (dc >> 1) + (h >> 1);
-      const bool odd = dc & 1;
+      // bf16: dims 8dc.. live in lane gq = dc % 8, M-blocks 4(dc/8)..; FP8:
+      // lane gq = dc/2, M-blocks 4(dc%2)..
+      const int src = F8 ? 4 * (dc >> 1) + (h >> 1) : 4 * (dc & 7) + (h >> 1);
+      const bool odd = F8 ? (dc & 1) : (dc >> 3);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float x0 = __shfl_sync(kFull, oacc[e][h & 1], src);
@@ -772,11 +773,11 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
   for (; it < n_units; ++it) {
     const int stage = it % NS;
     const uint32_t parity = (it / NS) & 1;
-    if (!mbar_wait(&R.bar[stage], parity)) {
+    if (!mbar_wait(&M.bar[stage], parity)) {
       timed_out = true;
       break;
     }
-    const StageDesc d = R.desc[stage];
+    const StageDesc d = M.desc[stage];
     const int u = u_begin + it;
     if (d.row != cur_row || d.item != cur_item) {
       if (cur_row >= 0) flush_segment();
@@ -794,7 +795,7 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
       // V rows 2tq, 2tq+1, 2tq+8, 2tq+9, codes of dims 16gq..16gq+15 (chunk gq)
       uint4 va = swz(Vp, 2 * tq, gq), vb = swz(Vp, 2 * tq + 1, gq);
       uint4 vc = swz(Vp, 2 * tq + 8, gq), vd = swz(Vp, 2 * tq + 9, gq);
-      const uint4 ksc = R.sc[stage][0], vsc = R.sc[stage][1];
+      const uint4 ksc = M.sc[stage][0], vsc = M.sc[stage][1];
       // The page now lives in registers: hand the stage back to the copy engine.
       __syncwarp();
       if (it + NS < n_units) {
@@ -928,23 +929,22 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
       }
     } else {
       // ---- bf16 pages on MMA fragments (same lane roles as FP8) ----
-      const uint8_t* Kp = reinterpret_cast<const uint8_t*>(R.kv[stage][0]);  // [16][256 B]
-      const uint8_t* Vp = reinterpret_cast<const uint8_t*>(R.kv[stage][1]);
-      // K rows gq, gq+8: dims 32tq..32tq+31 (64 bytes each)
+      const uint8_t* Kp = R.kv[stage][0];  // 32 swizzled units: token r = units 2r, 2r+1
+      const uint8_t* Vp = R.kv[stage][1];
+      // K rows gq, gq+8: dims 32tq..32tq+31 = unit half tq/2, chunks 4(tq%2)..+3
       uint4 ka[4], kb[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        ka[c] = *reinterpret_cast<const uint4*>(Kp + gq * 256 + tq * 64 + c * 16);
-        kb[c] = *reinterpret_cast<const uint4*>(Kp + (gq + 8) * 256 + tq * 64 + c * 16);
+        ka[c] = swz(Kp, 2 * gq + (tq >> 1), 4 * (tq & 1) + c);
+        kb[c] = swz(Kp, 2 * (gq + 8) + (tq >> 1), 4 * (tq & 1) + c);
       }
-      // V rows 2tq, 2tq+1, 2tq+8, 2tq+9: dims 16gq..16gq+15 (32 bytes each)
+      // V rows tq, tq+4, tq+8, tq+12: dims 8gq..8gq+7 (chunk gq of the first
+      // unit) and 64+8gq..64+8gq+7 (chunk gq of the second)
       uint4 vr[4][2];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        vr[0][c] = *reinterpret_cast<const uint4*>(Vp + (2 * tq) * 256 + gq * 32 + c * 16);
-        vr[1][c] = *reinterpret_cast<const uint4*>(Vp + (2 * tq + 1) * 256 + gq * 32 + c * 16);
-        vr[2][c] = *reinterpret_cast<const uint4*>(Vp + (2 * tq + 8) * 256 + gq * 32 + c * 16);
-        vr[3][c] = *reinterpret_cast<const uint4*>(Vp + (2 * tq + 9) * 256 + gq * 32 + c * 16);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) vr[x][c] = swz(Vp, 2 * (tq + 4 * x) + c, gq);
       }
       __syncwarp();
       if (it + NS < n_units) {
@@ -1003,7 +1003,8 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
       l2[0] += p0 + p2;
       l2[1] += p1 + p3;
       const uint32_t pe = pack_bf16x2(p0, p2), po = pack_bf16x2(p1, p3);
-      const int src0 = 8 * tq + (gq >> 1), src1 = src0 + 4;
+      // P^T operand: head gq, tokens tq, tq+4 (b0) and tq+8, tq+12 (b1)
+      const int src0 = 4 * tq + (gq >> 1), src1 = src0 + 16;
       const uint32_t x0 = __shfl_sync(kFull, pe, src0), x1 = __shfl_sync(kFull, po, src0);
       const uint32_t y0 = __shfl_sync(kFull, pe, src1), y1 = __shfl_sync(kFull, po, src1);
       const uint32_t X = (gq & 1) ? x1 : x0, Y = (gq & 1) ? y1 : y0;
@@ -1013,14 +1014,13 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
       // ---- O^T += V^T . P^T (rows past the sequence may hold anything) ----
       if (nvalid < kPage) {
         const uint4 z = make_uint4(0, 0, 0, 0);
-        if (2 * tq >= nvalid) vr[0][0] = vr[0][1] = z;
-        if (2 * tq + 1 >= nvalid) vr[1][0] = vr[1][1] = z;
-        if (2 * tq + 8 >= nvalid) vr[2][0] = vr[2][1] = z;
-        if (2 * tq + 9 >= nvalid) vr[3][0] = vr[3][1] = z;
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+          if (tq + 4 * x >= nvalid) vr[x][0] = vr[x][1] = z;
       }
 #pragma unroll
       for (int mb = 0; mb < 8; ++mb) {
-        // word mb of the 32 bytes of each row: dims 16gq+2mb, +1
+        // word mb % 4 of chunk mb / 4: dims 64(mb/4) + 8gq + 2(mb%4), +1
         const int k = mb & 3, hv = mb >> 2;
         auto word = [&](const uint4& x) { return k == 0 ? x.x : (k == 1 ? x.y : (k == 2 ? x.z : x.w)); };
         const uint32_t A = word(vr[0][hv]), B = word(vr[1][hv]), Cw = word(vr[2][hv]), Dw = word(vr[3][hv]);
@@ -1034,7 +1034,7 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
     if (lane == 0) flag_status(p.status, PKV_STATUS_TIMEOUT);
     // let copies still in flight land before the CTA's shared memory is released
     for (int k = it; k < min(n_units, it + NS); ++k)
-      mbar_wait(&R.bar[k % NS], (k / NS) & 1, kDrainLimitNs);
+      mbar_wait(&M.bar[k % NS], (k / NS) & 1, kDrainLimitNs);
     return;
   }
   if (cur_row >= 0) flush_segment();
@@ -1050,7 +1050,7 @@ static int variant_of(int gh) { return gh == 4 ? 2 : gh - 1; }
 // ([B+1] each) and seq_lens ([B]).
 template <bool F8>
 static size_t decode_smem_bytes(int num_seqs) {
-  return (F8 ? 1024 : 0) + sizeof(DecRing<F8>) * (F8 ? kDecWarpsF8 : kDecWarps) +
+  return 1024 + (sizeof(DecRing<F8>) + sizeof(DecMeta<F8>)) * (F8 ? kDecWarpsF8 : kDecWarps) +
          sizeof(int) * (3 * size_t(num_seqs) + 2);
 }
 
@@ -1201,17 +1201,22 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   dp.chunks = chunks;
   dp.prefix_part = reinterpret_cast<const float*>(ws + L.prefix);
 
-  CUtensorMap tk{}, tv{};  // unused by the bf16 variant
-  if (a.fp8) {
-    // the pools as [rows][128 codes], one 16-row box per (page, kv head)
-    const cuuint64_t rows = cuuint64_t(d.num_blocks) * d.num_kv_heads * kPage;
-    if (rows > cuuint64_t(INT_MAX)) return PKV_ERR_RANGE;  // TMA row coordinates are int32
-    const cuuint64_t dims[2] = {cuuint64_t(kHeadDim), rows};
-    const cuuint64_t strides[1] = {cuuint64_t(kHeadDim)};
-    const cuuint32_t box[2] = {cuuint32_t(kHeadDim), cuuint32_t(kPage)};
-    if (!encode_tensor_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.k_cache, 2, dims, strides, box) ||
-        !encode_tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.v_cache, 2, dims, strides, box))
+  // the pools as [units][128 bytes], one box of a whole (page, kv head): 16
+  // units of E4M3 codes, or 32 units (two per token) of bf16
+  CUtensorMap tk{}, tv{};
+  {
+    const int upp = (a.fp8 ? kPageBytesF8 : kPageBytes) / 128;  // units per page
+    const cuuint64_t units = cuuint64_t(d.num_blocks) * d.num_kv_heads * upp;
+    if (units > cuuint64_t(INT_MAX)) return PKV_ERR_RANGE;  // TMA coordinates are int32
+    const cuuint64_t dims[2] = {cuuint64_t(a.fp8 ? 128 : 64), units};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {cuuint32_t(a.fp8 ? 128 : 64), cuuint32_t(upp)};
+    const CUtensorMapDataType dt = a.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!encode_tensor_map(&tk, dt, a.k_cache, 2, dims, strides, box) ||
+        !encode_tensor_map(&tv, dt, a.v_cache, 2, dims, strides, box))
       return PKV_ERR_LAUNCH;
+  }
+  if (a.fp8) {
     switch (GH) {
       case 1: return launch_decode<1, true>(ctx, dp, tk, tv);
       case 2: return launch_decode<2, true>(ctx, dp, tk, tv);
