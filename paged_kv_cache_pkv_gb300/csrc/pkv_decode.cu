@@ -110,6 +110,15 @@ struct DecMeta {
   uint64_t bar[F8 ? kDecStagesF8 : kDecStages];
 };
 
+// Atomic add with acquire-release semantics at GPU scope: publishes the
+// warp's partial (ordered before it by __syncwarp) and, for the last arrival,
+// makes every other warp's partial visible.
+__device__ __forceinline__ unsigned long long atom_add_acq_rel(unsigned long long* p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+
 // 2^(byte - 127) for a scale byte in [1, 254]; 0 for byte 0.
 __device__ __forceinline__ float scale_of(uint32_t byte) { return __uint_as_float(byte << 23); }
 
@@ -407,6 +416,12 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
 
   // ---- plan: per-sequence unit counts and their exclusive prefix ----------
   const int per_row = p.Hkv * p.nsub;
+  // Stamp this launch's epoch (count 0) into every arrival counter, a share
+  // per thread, so that arrivals are single atomic adds.  A counter is first
+  // hit when a warp finishes a split item, long after these stamps; an
+  // arrival that still sees an old epoch adds again once it is stamped.
+  for (int i = blockIdx.x * NT + threadIdx.x; i < p.T * per_row; i += gridDim.x * NT)
+    atomicExch(p.counters + i, p.epoch << 16);
   {
     const int tid = threadIdx.x;
     const int per = (p.B + NT - 1) / NT;
@@ -749,23 +764,25 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
     // arrival: the last warp of this (row, head group) merges all partials
     int last = 0;
     if (lane == 0) {
-      __threadfence();
       const int w0 = cur_item_start / chunk, w1 = (cur_item_start + npages - 1) / chunk;
       const unsigned long long nparts = static_cast<unsigned long long>(w1 - w0 + 1);
       unsigned long long* ctr = p.counters + size_t(cur_row) * per_row + cur_item;
-      unsigned long long cur = atomicAdd(ctr, 0ull);
-      unsigned long long nxt;
-      while (true) {
-        nxt = (cur >> 16) == p.epoch ? cur + 1 : ((p.epoch << 16) | 1ull);
-        const unsigned long long prev = atomicCAS(ctr, cur, nxt);
-        if (prev == cur) break;
-        cur = prev;
+      unsigned long long v = atom_add_acq_rel(ctr, 1ull);
+      const uint64_t t0 = global_ns();
+      while ((v >> 16) != p.epoch) {  // not stamped yet: the stamp overwrites this add
+        if (global_ns() - t0 > kWaitLimitNs) {
+          flag_status(p.status, PKV_STATUS_TIMEOUT);
+          break;
+        }
+        v = atom_add_acq_rel(ctr, 1ull);
       }
-      last = (nxt & 0xFFFFull) == nparts;
-      if (last) __threadfence();
+      last = (v >> 16) == p.epoch && (v & 0xFFFFull) + 1 == nparts;
     }
     last = __shfl_sync(kFull, last, 0);
-    if (last) merge_item<GH>(p, lane, cur_row, cur_h0, cur_item_start, npages, chunk);
+    if (last) {
+      __syncwarp();  // the lanes read the partials after lane 0's acquire
+      merge_item<GH>(p, lane, cur_row, cur_h0, cur_item_start, npages, chunk);
+    }
   };
 
   bool timed_out = false;
