@@ -8,36 +8,41 @@
 // keys 0 .. L-n+j (bottom-right causal), query head h reading kv head h/G.
 //
 // Design (GB300):
-//  * One CTA = one tile of 128 query rows: TM = 128/G query tokens x the G
-//    query heads of one kv head (row = token*G + head), so every K/V tile
-//    loaded serves all G heads of the group.
-//  * Q tile: two TMA boxes (64 dims each, 128-byte swizzle) from q viewed as
+//  * A Q tile is 128 query rows: TM = 128/G query tokens x the G query heads
+//    of one kv head (row = token*G + head), so every K/V tile loaded serves
+//    all G heads of the group.  One CTA holds two Q tiles (2*TM consecutive
+//    tokens) and streams each K/V tile once for both: the copy engine's bytes
+//    per tensor-core FLOP are halved, which is what limits a single tile.
+//  * Q tiles: two TMA boxes each (64 dims, 128-byte swizzle) from q viewed as
 //    [T][Hq][128].  K and V tiles of 128 keys = 8 pages, each page two TMA
 //    boxes of 16 rows x 64 dims from the pool viewed as [NB*Hkv*16][128];
 //    page ids come from the block table, pages past the sequence are skipped.
 //    K/V tiles are double-buffered: tile i+1 loads while tile i computes.
-//  * S = Q K^T: 8 tcgen05.mma (M=128, N=128, K=16, bf16 in, fp32 out) into
-//    one of two TMEM buffers (columns 0..127 / 128..255); both operands
+//  * S = Q K^T: per Q tile 8 tcgen05.mma (M=128, N=128, K=16, bf16 in, fp32
+//    out) into that tile's TMEM columns (0..127 / 128..255); both operands
 //    K-major in shared memory.
 //  * Softmax: threads t and t+128 own TMEM lane t%128 (query row t%128), 64
 //    score columns each: tcgen05.ld, bottom-right causal mask, exp2 against
 //    the running max in the log2 domain, row max exchanged through shared
 //    memory.  The running max only moves when a score exceeds it by more than
 //    kTau (then the pass is redone and O in TMEM is rescaled), so most tiles
-//    take one pass.  P is rounded to bf16 and stored into TMEM (two bf16 per
-//    32-bit column, row = lane), where the PV MMA reads its A operand: no
-//    shared-memory traffic for P.
-//  * O += P V: 8 tcgen05.mma (A from TMEM) into TMEM columns 256..383; V is
-//    the N-major (dims contiguous) operand in shared memory.  V rows past the sequence end are zeroed in
-//    shared memory first so stale pool contents cannot reach O.
-//  * Warp roles: warps 0-7 run the softmax; warp 8 loads K tiles, warp 9
-//    loads V tiles (each refills a buffer as soon as the MMA that read it is
-//    done, with the next tile's block ids prefetched), warp 10 issues every
-//    tcgen05.mma.  Pipeline: S(i+2) is computed while the softmax of tile i
-//    runs, PV(i) under the softmax of tile i+1.  Hand-offs are mbarriers:
-//    TMA complete_tx for K/V, tcgen05.commit for S done / PV done, 256
-//    softmax arrivals for P ready (one barrier per double buffer, so no wait
-//    ever targets a phase more than one behind).
+//    take one pass.  P is rounded to bf16 and stored into TMEM over the
+//    thread's own S columns (two bf16 per 32-bit column, row = lane), where
+//    the PV MMA reads its A operand: no shared-memory traffic for P.
+//  * O += P V: per Q tile 8 tcgen05.mma (A from TMEM) into TMEM columns
+//    256..383 / 384..511; V is the N-major (dims contiguous) operand in shared
+//    memory.  V rows past the sequence end are zeroed in shared memory first
+//    so stale pool contents cannot reach O.
+//  * Warp roles: warps 0-7 run the softmax of the two Q tiles in turn; warp 8
+//    loads K tiles, warp 9 loads V tiles (each refills a buffer as soon as
+//    the MMAs that read it are done, with the next tiles' block ids
+//    prefetched), warps 10 and 11 issue the tcgen05.mma of Q tile 0 and 1.
+//    Pipeline per K/V tile i: PV(0, i) and S(0, i+1) run under the softmax of
+//    Q tile 1, PV(1, i) and S(1, i+1) under the softmax of Q tile 0 for tile
+//    i+1 (the S MMA that overwrites P is issued after the PV that reads it).  Hand-offs are
+//    mbarriers: TMA complete_tx for K/V, tcgen05.commit for S done / PV
+//    done, 256 softmax arrivals for P ready (one barrier per Q tile, so no
+//    wait ever targets a phase more than one behind).
 //  * Every mbarrier wait is bounded; on expiry the CTA flags
 //    PKV_STATUS_TIMEOUT, lets its in-flight copies and MMAs land, frees TMEM
 //    and returns.
@@ -54,20 +59,20 @@
 namespace pkv {
 
 constexpr int kPfSoftmaxThreads = 256;  // two threads per query row (64 score columns each)
-constexpr int kPfThreads = kPfSoftmaxThreads + 96;  // + K-load, V-load and MMA warps
+constexpr int kPfThreads = kPfSoftmaxThreads + 128;  // + K-load, V-load and two MMA warps
 constexpr int kPfKeys = 128;          // keys per K/V tile (8 pages)
 constexpr int kPfPagesPerTile = kPfKeys / kPage;
-constexpr uint32_t kTmemCols = 512;   // S0 [0,128), S1 [128,256), O [256,384), P0 [384,448), P1 [448,512)
+constexpr uint32_t kTmemCols = 512;   // S/P of Q tile 0 [0,128), of tile 1 [128,256), O0 [256,384), O1 [384,512)
 constexpr float kPfTau = 8.0f;
 
 // Shared-memory map (offsets from a 1024-byte aligned base); P lives in TMEM.
 constexpr uint32_t kHalfTile = 128 * 128;          // 128 rows x 64 bf16 = 16 KiB
 // K and V tiles each have kKVBufs buffers: a tile's load is issued when the
-// MMA that read the same buffer kKVBufs tiles earlier is done, which covers
+// MMAs that read the same buffer kKVBufs tiles earlier are done, which covers
 // the load latency of 8 random pages (about 1.3 us) at the tile cadence.
-constexpr int kKVBufs = 3;
-constexpr uint32_t kOffQ = 0;                                    // [2 halves]
-constexpr uint32_t kOffK = kOffQ + 2 * kHalfTile;                // [bufs][2 halves]
+constexpr int kKVBufs = 2;
+constexpr uint32_t kOffQ = 0;                                    // [2 Q tiles][2 halves]
+constexpr uint32_t kOffK = kOffQ + 4 * kHalfTile;                // [bufs][2 halves]
 constexpr uint32_t kOffV = kOffK + 2 * kKVBufs * kHalfTile;      // [bufs][2 halves]
 constexpr uint32_t kOffMisc = kOffV + 2 * kKVBufs * kHalfTile;
 constexpr uint32_t kPfMisc = 1536;  // barriers, TMEM address, tile info, scan sums, row exchange
@@ -223,40 +228,44 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                        const __grid_constant__ CUtensorMap tm_v, PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = sm + kOffQ;
+  uint8_t* sQ = sm + kOffQ;  // [tile u][2 halves]
   uint8_t* sK = sm + kOffK;
   uint8_t* sV = sm + kOffV;
-  // misc region: 16 barrier slots, TMEM address, tile info, row exchange
-  constexpr int kBars = 7 + 4 * kKVBufs;
+  // misc region: barriers, TMEM address, tile info, scan sums, row exchange
+  constexpr int kBars = 7 + 6 * kKVBufs;
   static_assert(kBars * 8 <= 192 && 208 + 4 * (kPfThreads / 32) <= 256 && 256 + 2 * 128 * 4 <= kPfMisc,
                 "prefill misc region layout");
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffMisc);
-  uint64_t* bar_q = bars;                     // Q landed
-  uint64_t* bar_s = bars + 1;                 // [2] S of a tile computed into TMEM buffer b
-  uint64_t* bar_o = bars + 3;                 // [2] PV that read P buffer b done
-  uint64_t* bar_p = bars + 5;                 // [2] P buffer b written by the softmax (256 arrivals)
+  uint64_t* bar_q = bars;                     // both Q tiles landed
+  uint64_t* bar_s = bars + 1;                 // [2] S of Q tile u computed into its TMEM columns
+  uint64_t* bar_o = bars + 3;                 // [2] PV of Q tile u done
+  uint64_t* bar_p = bars + 5;                 // [2] P of Q tile u written by the softmax (256 arrivals)
   uint64_t* bar_k = bars + 7;                 // [kKVBufs] K tile landed in buffer b
   uint64_t* bar_v = bar_k + kKVBufs;          // [kKVBufs] V tile landed in buffer b
-  uint64_t* bar_kfree = bar_v + kKVBufs;      // [kKVBufs] the S MMA reading K buffer b is done
-  uint64_t* bar_vfree = bar_kfree + kKVBufs;  // [kKVBufs] the PV MMA reading V buffer b is done
+  uint64_t* bar_kfree = bar_v + kKVBufs;          // [kKVBufs][2] the S MMAs of Q tile u reading K buffer b are done
+  uint64_t* bar_vfree = bar_kfree + 2 * kKVBufs;  // [kKVBufs][2] the PV MMAs of Q tile u reading V buffer b are done
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 192);  // after 24 barrier slots
   int* s_info = reinterpret_cast<int*>(sm + kOffMisc + 200);  // b, t0
   int* s_scan = reinterpret_cast<int*>(sK);  // plan scratch (before any K tile lands)
   int* s_wsum = reinterpret_cast<int*>(sm + kOffMisc + 208);  // [warps] scan sums
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = blockIdx.x;  // kv head; blockIdx.y = tile (real tiles dispatch first)
+  const int g = blockIdx.x;  // kv head; blockIdx.y = query group (real groups dispatch first)
+  // query tokens of the CTA: two Q tiles of TM tokens x G heads (the shared-
+  // prefix pass keeps one tile per CTA: its key windows are short chunks)
+  const int TG = PREFIX ? p.TM : 2 * p.TM;
 
   // ---- plan: this CTA's query rows and key window ----------------------------
-  int b = -1, t0 = 0, q_tok0 = 0, kbeg = 0, nkv = 0, key_end = 0, n = 0, L = 0;
+  int b = -1, t0 = 0, q_tok0 = 0, kbeg = 0, nkv = 0, key_end = 0, n = 0, L = 0, nt = 2;
   const int32_t* bt_row = p.block_tables;  // shared prefix: any row; row 0
   if constexpr (PREFIX) {
-    const int qtiles = (p.T + p.TM - 1) / p.TM;
+    const int qgroups = (p.T + TG - 1) / TG;
     const int i = int(blockIdx.y);
-    if (i >= qtiles * p.chunks) return;
+    if (i >= qgroups * p.chunks) return;
     const int qt = i / p.chunks, c = i - qt * p.chunks;
     const int ntiles = (p.prefix_pages * kPage + kPfKeys - 1) / kPfKeys;
-    q_tok0 = qt * p.TM;
+    q_tok0 = qt * TG;
+    nt = 1;
     kbeg = c * p.chunk_tiles;
     nkv = min(p.chunk_tiles, ntiles - kbeg);
     key_end = p.prefix_pages * kPage;
@@ -271,9 +280,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int nn = q1 - qq0;
       const bool bad = qq0 < 0 || nn < 0 || q1 > p.T || nn > LL || LL < 0 ||
                        (LL + kPage - 1) / kPage > p.max_blocks || (bb == 0 && qq0 != 0);
-      const int tiles = (!bad && nn > p.split_max_q) ? (nn + p.TM - 1) / p.TM : 0;
-      s_scan[bb] = tiles;
-      local += tiles;
+      const int groups = (!bad && nn > p.split_max_q) ? (nn + TG - 1) / TG : 0;
+      s_scan[bb] = groups;
+      local += groups;
     }
     int incl = local;
 #pragma unroll
@@ -298,7 +307,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (tid == 0) s_scan[p.B] = total;
     __syncthreads();
     if (tid == 0) {
-      // heavier tiles (later sequences, later query blocks) first
+      // heavier groups (later sequences, later query blocks) first
       const int i = total - 1 - int(blockIdx.y);
       int bb = -1, tt = 0;
       if (i >= 0) {
@@ -308,21 +317,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (s_scan[mid] <= i) lo = mid; else hi = mid;
         }
         bb = lo;
-        tt = (i - s_scan[lo]) * p.TM;
+        tt = (i - s_scan[lo]) * TG;
       }
       s_info[0] = bb;
       s_info[1] = tt;
     }
     __syncthreads();
     b = s_info[0];
-    if (b < 0) return;  // no tile for this CTA (before any TMEM is taken)
+    if (b < 0) return;  // no work for this CTA (before any TMEM is taken)
     t0 = s_info[1];
     const int q0 = __ldg(p.qsl + b);
     n = __ldg(p.qsl + b + 1) - q0;
     L = __ldg(p.seq_lens + b);
     q_tok0 = q0 + t0;
+    nt = n - t0 > p.TM ? 2 : 1;
     key_end = L;
-    const int max_pos = L - n + min(n, t0 + p.TM) - 1;
+    const int max_pos = L - n + min(n, t0 + nt * p.TM) - 1;
     nkv = max_pos / kPfKeys + 1;
     bt_row = p.block_tables + int64_t(b) * p.max_blocks;
   }
@@ -330,11 +340,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   // ---- barriers and TMEM -----------------------------------------------------
   if (tid == 0) {
-    for (int i = 0; i < kBars; ++i) mbar_init(bars + i, 1);
-    // One barrier per P buffer: the softmax can be a tile ahead of the MMA
-    // lane, never two on the same buffer (it needs PV(i) before P(i+2)).
-    mbar_init(bar_p, kPfSoftmaxThreads);
-    mbar_init(bar_p + 1, kPfSoftmaxThreads);
+    // each barrier initialised once: P ready takes the 256 softmax arrivals,
+    // every other barrier one arrival (a TMA transaction or a commit)
+    for (int i = 0; i < kBars; ++i)
+      mbar_init(bars + i, (bars + i == bar_p || bars + i == bar_p + 1) ? kPfSoftmaxThreads : 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -347,13 +356,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  const uint32_t tmem_o = tmem + 256;
   const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;  // warp w reads TMEM lanes 32*(w%4)..
-  auto tmem_s = [&](int buf) { return tmem + uint32_t(buf) * 128; };
-  auto tmem_p = [&](int buf) { return tmem + 384 + uint32_t(buf) * 64; };
+  // Q tile u: S (fp32) and, over the same columns once S is consumed, P
+  // (bf16 pairs; the half of the row a softmax thread owns starts its P at
+  // the start of its own S columns); O of tile u at 256 + 128u
+  auto tmem_s = [&](int u) { return tmem + uint32_t(u) * 128; };
+  auto tmem_o = [&](int u) { return tmem + 256 + uint32_t(u) * 128; };
   const uint32_t idesc_s = idesc_bf16(128, 128, false);
   const uint32_t idesc_o = idesc_bf16(128, 128, true);
-  const int role = warp - kPfSoftmaxThreads / 32;  // 0: K loads, 1: V loads, 2: MMA; < 0 softmax
+  const int role = warp - kPfSoftmaxThreads / 32;  // 0: K loads, 1: V loads, 2 + u: MMA of Q tile u; < 0 softmax
 
   auto load_tile = [&](const CUtensorMap* map, uint8_t* base, uint64_t* bar, const int (&bids)[kPfPagesPerTile]) {
     int valid = 0;
@@ -376,20 +387,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   if (role == 0 || role == 1) {
     // ===== K or V producer (lane 0 issues; the warp fetches block ids) =====
-    // Buffer kt % kKVBufs is free once the MMA that read tile kt - kKVBufs is
-    // done (S for K, PV for V; each buffer has its own barrier, so no wait
-    // targets a phase more than one behind).  Block ids come in groups of four
-    // tiles, one page per lane, read a group ahead: a tile's copies never wait
-    // on a block-table read.
+    // Buffer kt % kKVBufs is free once the MMAs that read tile kt - kKVBufs
+    // are done (the S of every Q tile for K, their PV for V; each buffer has
+    // its own barrier, so no wait targets a phase more than one behind).
+    // Block ids come in groups of four tiles, one page per lane, read a group
+    // ahead: a tile's copies never wait on a block-table read.
     const CUtensorMap* map = role == 0 ? &tm_k : &tm_v;
     uint8_t* base0 = role == 0 ? sK : sV;
     uint64_t* bar_load = role == 0 ? bar_k : bar_v;
     uint64_t* bar_free = role == 0 ? bar_kfree : bar_vfree;
     if (role == 0 && lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
-      mbar_arrive_expect_tx(bar_q, 2 * kHalfTile);
-      for (int h = 0; h < 2; ++h)
-        tma_load_3d(sQ + h * kHalfTile, &tm_q, h * 64, g * p.G, q_tok0, bar_q);
+      mbar_arrive_expect_tx(bar_q, uint32_t(nt) * 2 * kHalfTile);
+      for (int u = 0; u < nt; ++u)
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sQ + (u * 2 + h) * kHalfTile, &tm_q, h * 64, g * p.G, q_tok0 + u * p.TM, bar_q);
     }
     // lane l: page l % 8 of tile 4 * grp + l / 8 of this CTA's window (-1 past it)
     auto group_id = [&](int grp) {
@@ -410,7 +422,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
       for (int j = 0; j < kPfPagesPerTile; ++j) ids[j] = __shfl_sync(0xffffffffu, cur_g, (kt & 3) * 8 + j);
       const int kb = kt % kKVBufs;
-      if (lane == 0 && kt >= kKVBufs) ok = mbar_wait(bar_free + kb, ((kt / kKVBufs) - 1) & 1);
+      // the buffer is free once the MMA lane of every Q tile released it
+      if (lane == 0 && kt >= kKVBufs)
+        for (int u = 0; u < nt && ok; ++u) ok = mbar_wait(bar_free + kb * 2 + u, ((kt / kKVBufs) - 1) & 1);
       if (!__shfl_sync(0xffffffffu, int(ok), 0)) {
         ok = false;
         break;
@@ -425,226 +439,255 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (!ok) flag_status(p.status, PKV_STATUS_TIMEOUT);
     }
     __syncwarp();
-  } else if (role == 2) {
-    // ===== MMA issuer (one lane) =====
-    if (lane == 0) {
-      // S(kt): K buffer kt % kKVBufs -> TMEM S buffer kt & 1
+  } else if (role >= 2) {
+    // ===== MMA issuers: one lane per Q tile =====
+    // Per K/V tile kt: PV(u, kt) as soon as P(u, kt) is written, then S(u,
+    // kt+1) into the same TMEM columns (issued after the PV that reads P
+    // there).  The two Q tiles have their own issuing warps, so one tile's
+    // hand-offs never hold up the other's MMAs.
+    const int u = role - 2;
+    if (lane == 0 && u < nt) {
       auto issue_s = [&](int kt) {
-        const int buf = kt & 1, kb = kt % kKVBufs;
+        const int kb = kt % kKVBufs;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const int h = ks >> 2, kk = ks & 3;
-          const uint64_t a = smem_desc(smem_u32(sQ + h * kHalfTile) + kk * 32, 16, 1024);
+          const uint64_t a = smem_desc(smem_u32(sQ + (u * 2 + h) * kHalfTile) + kk * 32, 16, 1024);
           const uint64_t bdesc = smem_desc(smem_u32(sK + (kb * 2 + h) * kHalfTile) + kk * 32, 16, 1024);
-          umma(tmem_s(buf), a, bdesc, idesc_s, ks > 0);
+          umma(tmem_s(u), a, bdesc, idesc_s, ks > 0);
         }
-        umma_commit(bar_s + buf);
-        umma_commit(bar_kfree + kb);
+        umma_commit(bar_s + u);
+        umma_commit(bar_kfree + kb * 2 + u);
       };
-      int ns = 0, npv = 0;
-      bool ok = mbar_wait(bar_q, 0);
-      for (; ok && ns < min(2, nkv); ++ns) {
-        if (!(ok = mbar_wait(bar_k + ns, 0))) break;
-        issue_s(ns);
+      int ns = 0, npv = 0;  // S and PV groups issued (for the drain on failure)
+      bool ok = mbar_wait(bar_q, 0) && mbar_wait(bar_k, 0);
+      if (ok) {
+        issue_s(0);
+        ++ns;
       }
       for (int it = 0; ok && it < nkv; ++it) {
-        const int buf = it & 1, ph = (it >> 1) & 1, vb = it % kKVBufs;
-        // P(it) written by the softmax (which also released S buffer buf); V(it) landed
-        if (!(ok = mbar_wait(bar_p + buf, ph) && mbar_wait(bar_v + vb, (it / kKVBufs) & 1))) break;
+        const int vb = it % kKVBufs;
+        // P(u, it) written by the softmax; V(it) landed
+        if (!(ok = mbar_wait(bar_p + u, it & 1) && mbar_wait(bar_v + vb, (it / kKVBufs) & 1))) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {  // 16 keys = 8 packed TMEM columns of P
           const uint64_t bdesc = smem_desc(smem_u32(sV + vb * 2 * kHalfTile) + ks * 2048, kHalfTile, 1024);
-          umma_ts(tmem_o, tmem_p(buf) + ks * 8, bdesc, idesc_o, (it > 0 || ks > 0) ? 1u : 0u);
+          umma_ts(tmem_o(u), tmem_s(u) + (ks >> 2) * 64 + (ks & 3) * 8, bdesc, idesc_o,
+                  (it > 0 || ks > 0) ? 1u : 0u);
         }
-        umma_commit(bar_o + buf);
-        umma_commit(bar_vfree + vb);
+        umma_commit(bar_o + u);
+        umma_commit(bar_vfree + vb * 2 + u);
         ++npv;
-        if (ns < nkv) {  // ns == it + 2
-          if (!(ok = mbar_wait(bar_k + ns % kKVBufs, (ns / kKVBufs) & 1))) break;
-          issue_s(ns++);
+        if (it + 1 < nkv) {
+          if (!(ok = mbar_wait(bar_k + (it + 1) % kKVBufs, ((it + 1) / kKVBufs) & 1))) break;
+          issue_s(it + 1);
+          ++ns;
         }
       }
       if (!ok) {
         flag_status(p.status, PKV_STATUS_TIMEOUT);
-        // the newest commit of each kind lands before TMEM is released
-        for (int k = max(0, ns - 2); k < ns; ++k) mbar_wait(bar_s + (k & 1), (k >> 1) & 1, kDrainLimitNs);
-        for (int k = max(0, npv - 2); k < npv; ++k) mbar_wait(bar_o + (k & 1), (k >> 1) & 1, kDrainLimitNs);
+        // this lane's newest commits land before TMEM is released
+        if (ns > 0) mbar_wait(bar_s + u, (ns - 1) & 1, kDrainLimitNs);
+        if (npv > 0) mbar_wait(bar_o + u, (npv - 1) & 1, kDrainLimitNs);
       }
     }
     __syncwarp();
   } else {
-    // ===== softmax warps =====
+    // ===== softmax warps: Q tiles 0 and 1 in turn =====
     const int r = tid & 127;  // query row == TMEM lane
     const int ch = tid >> 7;  // which 64 of the 128 score columns
     const int t_rel = r / p.G;
-    // keys visible to this row: prefix pass sees the whole window
-    const bool row_valid = PREFIX ? q_tok0 + t_rel < p.T : t0 + t_rel < n;
-    const int pos = PREFIX ? key_end - 1 : (row_valid ? L - n + t0 + t_rel : L - 1);
-    float m = -INFINITY, l = 0.f;  // running max (same in both threads of a row), half row sum
+    // keys visible to row r of tile u: the prefix pass sees the whole window
+    bool row_valid[2];
+    int pos[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int tu = u * p.TM + t_rel;
+      row_valid[u] = u < nt && (PREFIX ? q_tok0 + tu < p.T : t0 + tu < n);
+      pos[u] = PREFIX ? key_end - 1 : (row_valid[u] ? L - n + t0 + tu : L - 1);
+    }
+    // running max (same in both threads of a row) and half row sum, per tile
+    float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
     float* s_red = reinterpret_cast<float*>(sm + kOffMisc + 256);  // [2][128] exchange
     bool ok = true;
-    for (int it = 0; it < nkv; ++it) {
-      const int buf = it & 1, ph = (it >> 1) & 1;
-      ok = mbar_wait(bar_s + buf, ph);
-      // TMEM P buffer `buf` was last read by PV(it-2)
-      if (it >= 2) ok = ok && mbar_wait(bar_o + buf, ph ^ 1);
-      tc_fence_after();
-      // ---- this thread's 64 columns of row r ----
-      const int kbase = (kbeg + it) * kPfKeys + ch * 64;
-      // no masking in this half tile for any row of the warp: the pass below
-      // runs warp-collective TMEM loads, so the choice must be warp-uniform
-      const bool full = __all_sync(0xffffffffu, kbase + 63 <= pos);
-      const uint32_t scol = tmem_s(buf) + lane_off + ch * 64;
-      uint32_t pk[2][16];
-      float mx = -INFINITY, rs = 0.f;
-      // One pass over the 64 columns: exp2(s*scale - mref) packed to bf16,
-      // optionally tracking the raw maximum.  FULL: no key of this half tile
-      // is past the row's position (no masking work at all).
-      auto pass = [&](float mref, auto full_t, auto track_t) {
-        constexpr bool FULL = decltype(full_t)::value, TRACK = decltype(track_t)::value;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        float mxl[2] = {-INFINITY, -INFINITY};
+    for (int it = 0; it < nkv && ok; ++it) {
+      for (int u = 0; u < nt; ++u) {
+        const int ph = it & 1;
+        const int posu = u ? pos[1] : pos[0];
+        float m = u ? m1 : m0;
+        ok = mbar_wait(bar_s + u, ph) && ok;
+        tc_fence_after();
+        // ---- this thread's 64 columns of row r ----
+        const int kbase = (kbeg + it) * kPfKeys + ch * 64;
+        // no masking in this half tile for any row of the warp: the pass below
+        // runs warp-collective TMEM loads, so the choice must be warp-uniform
+        const bool full = __all_sync(0xffffffffu, kbase + 63 <= posu);
+        const uint32_t scol = tmem_s(u) + lane_off + ch * 64;
+        uint32_t pk[2][16];
+        float mx = -INFINITY, rs = 0.f;
+        // One pass over the 64 columns: exp2(s*scale - mref) packed to bf16,
+        // optionally tracking the raw maximum.  FULL: no key of this half tile
+        // is past the row's position (no masking work at all).
+        auto pass = [&](float mref, auto full_t, auto track_t) {
+          constexpr bool FULL = decltype(full_t)::value, TRACK = decltype(track_t)::value;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          float mxl[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t sv[32];
-          tmem_ld32(scol + c * 32, sv);
-          tmem_wait_ld();
+          for (int c = 0; c < 2; ++c) {
+            uint32_t sv[32];
+            tmem_ld32(scol + c * 32, sv);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              float x0 = __uint_as_float(sv[2 * e]), x1 = __uint_as_float(sv[2 * e + 1]);
+              if constexpr (!FULL) {
+                const int k = kbase + c * 32 + 2 * e;
+                if (k > posu) x0 = -INFINITY;
+                if (k + 1 > posu) x1 = -INFINITY;
+              }
+              if constexpr (TRACK) {
+                mxl[0] = fmaxf(mxl[0], x0);
+                mxl[1] = fmaxf(mxl[1], x1);
+              }
+              const float a0 = ex2(fmaf(x0, p.qscale, -mref));  // exp2(-inf) = 0
+              const float a1 = ex2(fmaf(x1, p.qscale, -mref));
+              acc[e & 3] += a0 + a1;
+              pk[c][e] = pack_bf16x2(a0, a1);
+            }
+          }
+          rs = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+          if constexpr (TRACK) mx = fmaxf(mxl[0], mxl[1]);
+        };
+        if (full) pass(m, std::true_type{}, std::true_type{});
+        else pass(m, std::false_type{}, std::true_type{});
+        s_red[ch * 128 + r] = mx;
+        named_sync(1, kPfSoftmaxThreads);
+        const float row_mx = fmaxf(s_red[r], s_red[128 + r]) * p.qscale;
+        // s_red may be rewritten next tile; a failed wait anywhere stops every
+        // softmax thread here, together
+        if (named_sync_or(2, kPfSoftmaxThreads, !ok)) {
+          ok = false;
+          break;
+        }
+        const bool grow = row_mx > m + kPfTau;
+        float alpha = 1.f;
+        if (grow) {
+          alpha = m == -INFINITY ? 0.f : ex2(m - row_mx);
+          m = row_mx;
+        }
+        const bool warp_grow = __any_sync(0xffffffffu, grow);
+        // redo the pass against the new maximum; warp-uniform (TMEM loads are
+        // warp-collective), rows whose maximum did not move recompute the same P
+        if (warp_grow) {
+          if (full) pass(m, std::true_type{}, std::false_type{});
+          else pass(m, std::false_type{}, std::false_type{});
+        }
+        if (u) {
+          m1 = m;
+          l1 = l1 * alpha + rs;
+        } else {
+          m0 = m;
+          l0 = l0 * alpha + rs;
+        }
+        // P (bf16 pairs) over this thread's own S columns: row r, keys
+        // ch*64 .. ch*64+63 = 32 columns from the start of its half.  The
+        // other thread of the row may still read its S half; this one is done
+        // with its own.
+        {
+          uint32_t pw[32];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            float x0 = __uint_as_float(sv[2 * e]), x1 = __uint_as_float(sv[2 * e + 1]);
-            if constexpr (!FULL) {
-              const int k = kbase + c * 32 + 2 * e;
-              if (k > pos) x0 = -INFINITY;
-              if (k + 1 > pos) x1 = -INFINITY;
-            }
-            if constexpr (TRACK) {
-              mxl[0] = fmaxf(mxl[0], x0);
-              mxl[1] = fmaxf(mxl[1], x1);
-            }
-            const float a0 = ex2(fmaf(x0, p.qscale, -mref));  // exp2(-inf) = 0
-            const float a1 = ex2(fmaf(x1, p.qscale, -mref));
-            acc[e & 3] += a0 + a1;
-            pk[c][e] = pack_bf16x2(a0, a1);
+            pw[e] = pk[0][e];
+            pw[16 + e] = pk[1][e];
+          }
+          tmem_st32(scol, pw);
+          tmem_wait_st();
+        }
+        // rescale this thread's 64 O columns when the running max moved; O is
+        // final up to PV(u, it-1), which must have finished
+        if (it > 0 && warp_grow) {
+          const bool done = mbar_wait(bar_o + u, (it - 1) & 1);
+          ok = ok && done;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tmem_o(u) + lane_off + ch * 64 + c * 32, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st32(tmem_o(u) + lane_off + ch * 64 + c * 32, ov);
+          }
+          tmem_wait_st();
+        }
+        // keys past the sequence end: zero their V rows (after V landed, once
+        // per K/V tile, before the first PV reads them) so stale pool contents
+        // cannot leak through P = 0
+        if (u == 0 && (kbeg + it + 1) * kPfKeys > key_end) {
+          const int vb = it % kKVBufs;
+          ok = mbar_wait(bar_v + vb, (it / kKVBufs) & 1) && ok;
+          if ((kbeg + it) * kPfKeys + r >= key_end) {
+            uint4* vrow = reinterpret_cast<uint4*>(sV + (vb * 2 + ch) * kHalfTile + r * 128);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) vrow[q] = make_uint4(0, 0, 0, 0);
           }
         }
-        rs = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-        if constexpr (TRACK) mx = fmaxf(mxl[0], mxl[1]);
-      };
-      if (full) pass(m, std::true_type{}, std::true_type{});
-      else pass(m, std::false_type{}, std::true_type{});
-      s_red[ch * 128 + r] = mx;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar_p + u);  // P(u, it) is ready for the MMA warp
+      }
+    }
+    // ---- epilogue per Q tile: O / l -> bf16, each thread its 64 columns of row r ----
+    for (int u = 0; u < nt; ++u) {
+      ok = ok && mbar_wait(bar_o + u, (nkv - 1) & 1);
+      named_sync(1, kPfSoftmaxThreads);  // s_red of the previous use is read
+      s_red[ch * 128 + r] = u ? l1 : l0;
       named_sync(1, kPfSoftmaxThreads);
-      const float row_mx = fmaxf(s_red[r], s_red[128 + r]) * p.qscale;
-      // s_red may be rewritten next tile; a failed wait anywhere stops every
-      // softmax thread here, together
-      if (named_sync_or(2, kPfSoftmaxThreads, !ok)) {
-        ok = false;
-        break;
-      }
-      const bool grow = row_mx > m + kPfTau;
-      float alpha = 1.f;
-      if (grow) {
-        alpha = m == -INFINITY ? 0.f : ex2(m - row_mx);
-        m = row_mx;
-      }
-      const bool warp_grow = __any_sync(0xffffffffu, grow);
-      // redo the pass against the new maximum; warp-uniform (TMEM loads are
-      // warp-collective), rows whose maximum did not move recompute the same P
-      if (warp_grow) {
-        if (full) pass(m, std::true_type{}, std::false_type{});
-        else pass(m, std::false_type{}, std::false_type{});
-      }
-      l = l * alpha + rs;
-      // P (bf16 pairs) into TMEM: row r, keys ch*64 .. ch*64+63 = 32 columns
-      {
-        uint32_t pw[32];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          pw[e] = pk[0][e];
-          pw[16 + e] = pk[1][e];
-        }
-        tmem_st32(tmem_p(buf) + lane_off + ch * 32, pw);
-        tmem_wait_st();
-      }
-      // rescale this thread's 64 O columns when the running max moved; O is
-      // final up to PV(it-1), which must have finished
-      if (it > 0 && warp_grow) {
-        const bool done = mbar_wait(bar_o + (buf ^ 1), ((it - 1) >> 1) & 1);
-        ok = ok && done;
-        tc_fence_after();
+      tc_fence_after();
+      const float lsum = s_red[r] + s_red[128 + r];
+      const int tok = q_tok0 + u * p.TM + t_rel;
+      const bool valid = (u ? row_valid[1] : row_valid[0]) && ok;
+      if constexpr (PREFIX) {
+        // partial record: o (unnormalised, 128 floats), running max m, sum l
+        float* rec = p.prefix_part + ((size_t(tok) * p.Hq + g * p.G + (r % p.G)) * p.chunks + b) * kPrefixRec;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t ov[32];
-          tmem_ld32(tmem_o + lane_off + ch * 64 + c * 32, ov);
+          tmem_ld32(tmem_o(u) + lane_off + ch * 64 + c * 32, ov);
           tmem_wait_ld();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(rec + ch * 64 + c * 32);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st32(tmem_o + lane_off + ch * 64 + c * 32, ov);
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(__uint_as_float(ov[4 * q]), __uint_as_float(ov[4 * q + 1]),
+                                   __uint_as_float(ov[4 * q + 2]), __uint_as_float(ov[4 * q + 3]));
+          }
         }
-        tmem_wait_st();
-      }
-      // keys past the sequence end: zero their V rows (after V landed) so
-      // stale pool contents cannot leak through P = 0
-      if ((kbeg + it + 1) * kPfKeys > key_end) {
-        const int vb = it % kKVBufs;
-        ok = mbar_wait(bar_v + vb, (it / kKVBufs) & 1) && ok;
-        if ((kbeg + it) * kPfKeys + r >= key_end) {
-          uint4* vrow = reinterpret_cast<uint4*>(sV + (vb * 2 + ch) * kHalfTile + r * 128);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) vrow[q] = make_uint4(0, 0, 0, 0);
+        if (valid && ch == 0) {
+          rec[128] = u ? m1 : m0;
+          rec[129] = lsum;
         }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar_p + buf);  // P of this tile is ready for the MMA warp
-    }
-    // ---- epilogue: O / l -> bf16, each thread its 64 columns of row r ----
-    ok = ok && mbar_wait(bar_o + ((nkv - 1) & 1), ((nkv - 1) >> 1) & 1);
-    s_red[ch * 128 + r] = l;
-    named_sync(1, kPfSoftmaxThreads);
-    tc_fence_after();
-    const float lsum = s_red[r] + s_red[128 + r];
-    if constexpr (PREFIX) {
-      // partial record: o (unnormalised, 128 floats), running max m, sum l
-      float* rec = p.prefix_part +
-                   ((size_t(q_tok0 + t_rel) * p.Hq + g * p.G + (r % p.G)) * p.chunks + b) * kPrefixRec;
+      } else {
+        const float inv = 1.f / lsum;
+        uint16_t* orow = p.out + (size_t(tok) * p.Hq + g * p.G + (r % p.G)) * kHeadDim + ch * 64;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(tmem_o + lane_off + ch * 64 + c * 32, ov);
-        tmem_wait_ld();
-        if (row_valid && ok) {
-          float4* dst = reinterpret_cast<float4*>(rec + ch * 64 + c * 32);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tmem_o(u) + lane_off + ch * 64 + c * 32, ov);
+          tmem_wait_ld();
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(ov[4 * q]), __uint_as_float(ov[4 * q + 1]),
-                                 __uint_as_float(ov[4 * q + 2]), __uint_as_float(ov[4 * q + 3]));
-        }
-      }
-      if (row_valid && ok && ch == 0) {
-        rec[128] = m;
-        rec[129] = lsum;
-      }
-    } else {
-      const float inv = 1.f / lsum;
-      uint16_t* orow = p.out + (size_t(q_tok0 + t_rel) * p.Hq + g * p.G + (r % p.G)) * kHeadDim + ch * 64;
+            for (int q = 0; q < 4; ++q) {
+              uint32_t w4[4];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(tmem_o + lane_off + ch * 64 + c * 32, ov);
-        tmem_wait_ld();
-        if (row_valid && ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w4[e] = pack_bf16x2(__uint_as_float(ov[8 * q + 2 * e]) * inv,
-                                  __uint_as_float(ov[8 * q + 2 * e + 1]) * inv);
-            dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              for (int e = 0; e < 4; ++e)
+                w4[e] = pack_bf16x2(__uint_as_float(ov[8 * q + 2 * e]) * inv,
+                                    __uint_as_float(ov[8 * q + 2 * e + 1]) * inv);
+              dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
           }
         }
       }
@@ -766,8 +809,11 @@ int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, void* /*scratch*/,
   CUtensorMap tq, tk, tv;
   if (int e = make_maps(a, &tq, &tk, &tv)) return e;
   const PrefillParams pp = make_params(ctx, a, split_max_q);
+  // one CTA per group of two Q tiles; every sequence may end in a partial group
+  const int tg = 2 * pp.TM;
+  const int groups = min(max_tiles, (a.num_tokens + tg - 1) / tg + a.num_seqs);
   TraceScope ts(ctx.stream, PKV_K_PREFILL);
-  pkv_prefill_kernel<false><<<dim3(a.desc.num_kv_heads, max_tiles), kPfThreads, kPfSmemBytes,
+  pkv_prefill_kernel<false><<<dim3(a.desc.num_kv_heads, groups), kPfThreads, kPfSmemBytes,
                               ctx.stream>>>(tq, tk, tv, pp);
   return ts.done();
 }
@@ -777,12 +823,12 @@ int prefix_chunks(const pkv_desc& d, int32_t num_tokens, int32_t prefix_pages, i
     *chunk_tiles = 0;
     return 0;
   }
-  const int tm = tile_tokens(d);
-  const int qtiles = (num_tokens + tm - 1) / tm;
+  const int tg = tile_tokens(d);  // query tokens per CTA of the prefix pass (one Q tile)
+  const int qgroups = (num_tokens + tg - 1) / tg;
   const int ntiles = (prefix_pages * kPage + kPfKeys - 1) / kPfKeys;
   // split the prefix keys until the pass has about one CTA per SM (152), at
   // most 16 chunks (the split-KV merge holds one chunk per lane of a half warp)
-  const int want = min(16, max(1, (152 + qtiles * d.num_kv_heads - 1) / (qtiles * d.num_kv_heads)));
+  const int want = min(16, max(1, (152 + qgroups * d.num_kv_heads - 1) / (qgroups * d.num_kv_heads)));
   const int per = max(1, (ntiles + want - 1) / want);
   *chunk_tiles = per;
   return (ntiles + per - 1) / per;
@@ -798,9 +844,9 @@ int launch_prefix(const LaunchCtx& ctx, const AttendArgs& a, float* records, int
   pp.chunk_tiles = chunk_tiles;
   pp.chunks = chunks;
   pp.prefix_part = records;
-  const int qtiles = (a.num_tokens + pp.TM - 1) / pp.TM;
+  const int qgroups = (a.num_tokens + pp.TM - 1) / pp.TM;
   TraceScope ts(ctx.stream, PKV_K_PREFILL);
-  pkv_prefill_kernel<true><<<dim3(a.desc.num_kv_heads, qtiles * chunks), kPfThreads, kPfSmemBytes,
+  pkv_prefill_kernel<true><<<dim3(a.desc.num_kv_heads, qgroups * chunks), kPfThreads, kPfSmemBytes,
                              ctx.stream>>>(tq, tk, tv, pp);
   return ts.done();
 }
