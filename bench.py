@@ -411,6 +411,8 @@ def main():
                          "avg_launch_us": dec_avg_s * 1e6,
                          "timing": "CUDA events around each launch, traced pass of the same steps"},
             "kernels": per_kernel,
+            "step_us": {"median": 1e3 * float(np.median(step_ms)), "p10": 1e3 * float(np.percentile(step_ms, 10)),
+                        "p90": 1e3 * float(np.percentile(step_ms, 90))},
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu,

@@ -145,6 +145,13 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
+// Hint: bring `bytes` (a multiple of 16, 16-byte aligned) at `src` into L2.
+// L2 is the GPU's point of coherence, so a prefetch can never expose stale data
+// to a later read.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Bulk (non-tensor) async copy global -> shared, completing on an mbarrier.
 // dst/src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,

@@ -521,6 +521,22 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
       }
     }
   };
+  // The first pages of the ring into L2 while the previous kernel (normally
+  // pkv_write) is still running; the copies into shared memory wait below.
+  // (bf16 pages: 1 % on the 8B-shaped batch; the FP8 variant ran 2 % slower.)
+  if constexpr (!F8) {
+    Cursor c = pc;
+    const int npf = min(NS, n_units);
+    for (int s = 0; s < npf; ++s) {
+      if (lane == 0) {
+        constexpr int PB = kPageBytesOf<F8>;
+        const size_t ph = size_t(c.bid) * p.Hkv + c.item / p.nsub;
+        prefetch_l2(p.k_cache + ph * PB, PB);
+        prefetch_l2(p.v_cache + ph * PB, PB);
+      }
+      if (s + 1 < npf) cursor_advance(c, p, sq, per_row);
+    }
+  }
   griddep_wait();
   {
     const int prologue = min(NS, n_units);

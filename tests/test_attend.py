@@ -207,7 +207,7 @@ def test_long_chunks_run_on_the_tensor_core_kernel(pkvlib):
 
 
 @pytest.mark.parametrize("hq,hkv,L,n", [(32, 8, 1100, 130), (16, 2, 257, 257), (8, 8, 640, 300),
-                                        (32, 2, 129, 33), (64, 4, 3000, 17)])
+                                        (32, 2, 129, 33), (64, 4, 3000, 17), (32, 8, 2000, 100)])
 def test_prefill_chunks_all_rows(pkvlib, hq, hkv, L, n):
     """Chunks spanning several 128-key tiles with ragged ends, every row."""
     b = make_batch([L, 40], [n, 1], hq, hkv, seed=L + n, device="cuda")
@@ -215,6 +215,16 @@ def test_prefill_chunks_all_rows(pkvlib, hq, hkv, L, n):
     assert counts["prefill"] == 1
     k_ref, v_ref = oracle_write(b)
     compare(out, oracle_attend(b, k_ref, v_ref), what=f"prefill {hq}/{hkv} L={L} n={n}")
+
+
+def test_prefill_chunks_of_several_sequences(pkvlib):
+    """Several prefill chunks in one step: query groups of two Q tiles per CTA,
+    a last group with one tile or with a partial second tile, next to decode rows."""
+    b = make_batch([2000, 1500, 64, 700, 333], [300, 77, 1, 36, 33], 32, 8, seed=77, device="cuda")
+    counts, out, _, _ = _kernel_launches(b, 300)
+    assert counts["prefill"] == 1
+    k_ref, v_ref = oracle_write(b)
+    compare(out, oracle_attend(b, k_ref, v_ref), what="several prefill chunks")
 
 
 def _cascade(batch, prefix_pages, max_query_len=0):
