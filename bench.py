@@ -278,7 +278,8 @@ def main():
     def step():
         if fp8:
             pkv.write_fp8(b.k_new, b.v_new, slots, kc, vc, ks, vs)
-            pkv.attend_fp8(b.q, kc, vc, ks, vs, bt, lens, qsl, b.scale, out=out, workspace=ws)
+            pkv.attend_fp8(b.q, kc, vc, ks, vs, bt, lens, qsl, b.scale, out=out, workspace=ws,
+                           max_query_len=max_q)
             return
         pkv.write(b.k_new, b.v_new, slots, kc, vc)
         pkv.attend(b.q, kc, vc, bt, lens, qsl, b.scale, out=out, workspace=ws, max_query_len=max_q,
@@ -376,7 +377,7 @@ def main():
         if fp8:
             pkv.write_fp8(dev_in["k_new"], dev_in["v_new"], dev_in["slots"], kc, vc, ks, vs)
             pkv.attend_fp8(dev_in["q"], kc, vc, ks, vs, dev_in["bt"], dev_in["lens"], dev_in["qsl"],
-                           b.scale, out=out, workspace=ws)
+                           b.scale, out=out, workspace=ws, max_query_len=max_q)
         else:
             pkv.write(dev_in["k_new"], dev_in["v_new"], dev_in["slots"], kc, vc)
             pkv.attend(dev_in["q"], kc, vc, dev_in["bt"], dev_in["lens"], dev_in["qsl"], b.scale, out=out,

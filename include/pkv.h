@@ -241,17 +241,21 @@ PKV_API int pkv_attend_fp8_workspace_size(const pkv_desc* desc, int32_t num_seqs
                                           int32_t num_tokens, size_t* bytes);
 
 /* pkv_attend_fp8 -- pkv_attend over FP8 pages: the same result with K and V
- * the exact values code * 2^(scale - 127).  Every query row runs on the
- * split-KV kernel (no tensor-core prefill and no shared-prefix cascade for
- * FP8 pages).  workspace: at least pkv_attend_fp8_workspace_size(desc,
- * num_seqs, num_tokens) bytes, 256-byte aligned, no initialisation needed.  Scale bytes of rows a query sees must lie in
- * [1, 254] (pkv_write_fp8 writes nothing else); rows it does not see are
- * never used, whatever they hold. */
+ * the exact values code * 2^(scale - 127).  Query chunks longer than
+ * PKV_SPLITKV_MAX_QLEN run on the tensor-core prefill kernel (the pages
+ * widened exactly to bf16 in shared memory), the rest on split-KV, as in
+ * pkv_attend; max_query_len has pkv_attend's meaning.  No shared-prefix
+ * cascade for FP8 pages.  workspace: at least
+ * pkv_attend_fp8_workspace_size(desc, num_seqs, num_tokens) bytes, 256-byte
+ * aligned, no initialisation needed.  Scale bytes of rows a query sees must
+ * lie in [1, 254] (pkv_write_fp8 writes nothing else); rows it does not see
+ * are never used, whatever they hold. */
 PKV_API int pkv_attend_fp8(const pkv_bf16* q, const pkv_fp8* k_cache,
                            const pkv_fp8* v_cache, const uint8_t* k_scale,
                            const uint8_t* v_scale, const int32_t* block_tables,
                            const int32_t* seq_lens, const int32_t* query_start_loc,
-                           int32_t num_seqs, int32_t num_tokens, float scale,
+                           int32_t num_seqs, int32_t num_tokens, int32_t max_query_len,
+                           float scale,
                            pkv_bf16* out, void* workspace, size_t workspace_bytes,
                            const pkv_desc* desc, pkv_stream_t stream);
 

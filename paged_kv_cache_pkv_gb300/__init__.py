@@ -58,7 +58,7 @@ _SIGS = {
                                          ctypes.c_float, _vp, ctypes.POINTER(Desc), _vp]),
     "pkv_write_fp8": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, ctypes.POINTER(Desc), _vp]),
     "pkv_attend_fp8_workspace_size": (ctypes.c_int, [ctypes.POINTER(Desc), _i32, _i32, ctypes.POINTER(_sz)]),
-    "pkv_attend_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float,
+    "pkv_attend_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_float,
                                       _vp, _vp, _sz, ctypes.POINTER(Desc), _vp]),
     "pkv_get_last_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
     "pkv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -246,9 +246,10 @@ def workspace_size_fp8(desc, num_seqs, num_tokens, device=None):
 
 
 def attend_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, query_start_loc, scale,
-               out=None, workspace=None, stream=None):
+               out=None, workspace=None, stream=None, max_query_len=0):
     """attend() over FP8 pages (codes and per-row scale bytes as written by
-    write_fp8); every query row runs on the split-KV kernel."""
+    write_fp8): long query chunks on the tensor-core prefill kernel, the rest
+    on split-KV; max_query_len as in attend() (0: unknown)."""
     _need(q, "q", torch.bfloat16, 3)
     _need_fp8_pool(k_cache, v_cache, k_scale, v_scale)
     _need(block_tables, "block_tables", torch.int32, 2)
@@ -277,7 +278,8 @@ def attend_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, qu
     with torch.cuda.device(q.device):
         _check(lib().pkv_attend_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                     _ptr(block_tables), _ptr(seq_lens), _ptr(query_start_loc), B, T,
-                                    float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                                    int(max_query_len), float(scale), _ptr(out), _ptr(workspace),
+                                    workspace.numel(),
                                     ctypes.byref(desc), _stream(q.device, stream)),
                "pkv_attend_fp8")
     return out

@@ -1191,10 +1191,9 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   if (a.workspace_bytes < L.total) return PKV_ERR_WORKSPACE;
   if (a.num_tokens == 0 || a.num_seqs == 0) return PKV_OK;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  // Long query chunks go to the tensor-core kernel unless the caller's bound
-  // says there are none; then split-KV takes every row.
-  // (FP8 pages: split-KV takes every row)
-  const bool prefill = !a.fp8 && max_tiles > 0 && a.num_tokens > simt_max_q() &&
+  // Long query chunks go to the tensor-core kernel (bf16 or FP8 pages) unless
+  // the caller's bound says there are none; then split-KV takes every row.
+  const bool prefill = max_tiles > 0 && a.num_tokens > simt_max_q() &&
                        (a.max_query_len <= 0 || a.max_query_len > simt_max_q());
   const int split_max_q = prefill ? simt_max_q() : INT_MAX;
   if (prefill) {

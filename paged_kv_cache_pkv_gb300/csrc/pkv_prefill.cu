@@ -48,6 +48,7 @@
 //    and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 
 #include <climits>
 #include <mutex>
@@ -74,10 +75,22 @@ constexpr int kKVBufs = 2;
 constexpr uint32_t kOffQ = 0;                                    // [2 Q tiles][2 halves]
 constexpr uint32_t kOffK = kOffQ + 4 * kHalfTile;                // [bufs][2 halves]
 constexpr uint32_t kOffV = kOffK + 2 * kKVBufs * kHalfTile;      // [bufs][2 halves]
-constexpr uint32_t kOffMisc = kOffV + 2 * kKVBufs * kHalfTile;
+constexpr uint32_t kOffMisc = kOffV + 2 * kKVBufs * kHalfTile;  // bf16 pages
+// FP8 pages: one K/V tile of E4M3 codes (8 pages of 16 rows x 128 codes, as
+// TMA lands them with 128-byte swizzle) and its 128 row scale bytes, for each
+// of K and V, staged before the misc region.
+constexpr uint32_t kStagePage = kPage * 128;
+constexpr uint32_t kOffStageK = kOffMisc;
+constexpr uint32_t kOffStageV = kOffStageK + kPfPagesPerTile * kStagePage;
+constexpr uint32_t kOffScK = kOffStageV + kPfPagesPerTile * kStagePage;
+constexpr uint32_t kOffScV = kOffScK + kPfPagesPerTile * kScaleBytes;
+constexpr uint32_t kOffMiscF8 = kOffScV + kPfPagesPerTile * kScaleBytes;
+template <bool F8>
+constexpr uint32_t kMiscOf = F8 ? kOffMiscF8 : kOffMisc;
 constexpr uint32_t kPfMisc = 1536;  // barriers, TMEM address, tile info, scan sums, row exchange
-constexpr uint32_t kPfSmemBytes = kOffMisc + kPfMisc + 1024;  // + alignment slack
-static_assert(kPfSmemBytes <= 232448, "prefill shared memory above the 227 KiB per-CTA limit");
+template <bool F8>
+constexpr uint32_t kPfSmemOf = kMiscOf<F8> + kPfMisc + 1024;  // + alignment slack
+static_assert(kPfSmemOf<true> <= 232448, "prefill shared memory above the 227 KiB per-CTA limit");
 
 struct PrefillParams {
   const int32_t* block_tables;
@@ -91,6 +104,9 @@ struct PrefillParams {
   // (common to every block-table row) in chunks of chunk_tiles key tiles
   int32_t prefix_pages, chunk_tiles, chunks;
   float* prefix_part;  // [T][Hq][chunks] records of kPrefixRec floats
+  // FP8 pages: row scale bytes [NB][Hkv][16] of K and V (null for bf16 pages)
+  const uint8_t* k_scale;
+  const uint8_t* v_scale;
 };
 
 // ---------------------------------------------------------------------------
@@ -215,13 +231,62 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Bulk copy global -> shared (16-byte aligned, a multiple of 16 bytes).
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Four E4M3 codes (lowest byte first) -> two f16x2 (exact: E4M3 is a subset of f16).
+__device__ __forceinline__ void e4m3x4_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// f16 pair times a power of two -> bf16 pair (exact for E4M3 values under the
+// row scales the FP8 write produces).
+__device__ __forceinline__ uint32_t widen_pair(uint32_t h2, float sc) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  return pack_bf16x2(f.x * sc, f.y * sc);
+}
+
+// One lane's half row of an FP8 page: codes of dims 64h..64h+63 of row r (the
+// staged page as TMA laid it out, 128-byte swizzle) times 2^(scale-127), as
+// bf16 into row `drow` of the half-h block of a K/V tile (128-byte swizzle,
+// row index = key within the tile, congruent to r mod 8).  The chunk order
+// c = cc ^ 4h keeps each quarter-warp's 16-byte stores on distinct banks.
+__device__ __forceinline__ void widen_row_half(const uint8_t* spage, uint32_t sbyte, uint8_t* drow,
+                                               int r, int h) {
+  uint4 c4[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    c4[i] = *reinterpret_cast<const uint4*>(spage + r * 128 + (((4 * h + i) ^ (r & 7)) << 4));
+  const float sc = __uint_as_float(sbyte << 23);  // 2^(sbyte-127); byte 0 is never written
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc) {
+    const int c = cc ^ (h << 2);  // dims 8c..8c+7 of the half
+    const uint4 src = c4[c >> 1];
+    const uint32_t w0 = (c & 1) ? src.z : src.x, w1 = (c & 1) ? src.w : src.y;
+    uint32_t a0, a1, a2, a3;
+    e4m3x4_f16x2(w0, a0, a1);
+    e4m3x4_f16x2(w1, a2, a3);
+    const uint4 o = make_uint4(widen_pair(a0, sc), widen_pair(a1, sc), widen_pair(a2, sc), widen_pair(a3, sc));
+    *reinterpret_cast<uint4*>(drow + ((c ^ (r & 7)) << 4)) = o;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // kernel
 // ---------------------------------------------------------------------------
 // PREFIX = false: chunked prefill (bottom-right causal, normalised output).
 // PREFIX = true: every query row against the shared prefix keys, written as
 // log-sum-exp partial records that the split-KV kernel merges.
-template <bool PREFIX>
+template <bool PREFIX, bool F8>
 __global__ void __launch_bounds__(kPfThreads, 1)
     pkv_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -232,10 +297,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint8_t* sK = sm + kOffK;
   uint8_t* sV = sm + kOffV;
   // misc region: barriers, TMEM address, tile info, scan sums, row exchange
-  constexpr int kBars = 7 + 6 * kKVBufs;
+  constexpr uint32_t kOffM = kMiscOf<F8>;
+  constexpr int kBars = 7 + 6 * kKVBufs + 2;
   static_assert(kBars * 8 <= 192 && 208 + 4 * (kPfThreads / 32) <= 256 && 256 + 2 * 128 * 4 <= kPfMisc,
                 "prefill misc region layout");
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffMisc);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffM);
   uint64_t* bar_q = bars;                     // both Q tiles landed
   uint64_t* bar_s = bars + 1;                 // [2] S of Q tile u computed into its TMEM columns
   uint64_t* bar_o = bars + 3;                 // [2] PV of Q tile u done
@@ -244,10 +310,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t* bar_v = bar_k + kKVBufs;          // [kKVBufs] V tile landed in buffer b
   uint64_t* bar_kfree = bar_v + kKVBufs;          // [kKVBufs][2] the S MMAs of Q tile u reading K buffer b are done
   uint64_t* bar_vfree = bar_kfree + 2 * kKVBufs;  // [kKVBufs][2] the PV MMAs of Q tile u reading V buffer b are done
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 192);  // after 24 barrier slots
-  int* s_info = reinterpret_cast<int*>(sm + kOffMisc + 200);  // b, t0
+  uint64_t* bar_kst = bar_vfree + 2 * kKVBufs;     // FP8: a K tile's codes and scales staged
+  uint64_t* bar_vst = bar_kst + 1;                 // FP8: a V tile's codes and scales staged
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffM + 192);  // after 24 barrier slots
+  int* s_info = reinterpret_cast<int*>(sm + kOffM + 200);  // b, t0
   int* s_scan = reinterpret_cast<int*>(sK);  // plan scratch (before any K tile lands)
-  int* s_wsum = reinterpret_cast<int*>(sm + kOffMisc + 208);  // [warps] scan sums
+  int* s_wsum = reinterpret_cast<int*>(sm + kOffM + 208);  // [warps] scan sums
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = blockIdx.x;  // kv head; blockIdx.y = query group (real groups dispatch first)
@@ -413,6 +481,38 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     int next_g = nkv > 4 ? group_id(1) : -1;
     int loaded = 0;
     bool ok = true;
+    // FP8 pages: the tile's codes and scales go to a staging area first (lane
+    // 0 issues), and the warp widens them into the bf16 tile buffer.
+    uint8_t* stage = sm + (role == 0 ? kOffStageK : kOffStageV);
+    uint8_t* ssc = sm + (role == 0 ? kOffScK : kOffScV);
+    const uint8_t* scl = role == 0 ? p.k_scale : p.v_scale;
+    uint64_t* bar_st = role == 0 ? bar_kst : bar_vst;
+    int st_pending = -1;  // tile whose staging copies are out and not yet waited for
+    auto arm_stage = [&](const int (&bids)[kPfPagesPerTile]) {
+      int valid = 0;
+#pragma unroll
+      for (int j = 0; j < kPfPagesPerTile; ++j) valid += bids[j] >= 0;
+      mbar_arrive_expect_tx(bar_st, uint32_t(valid) * (kStagePage + kScaleBytes));
+    };
+    auto stage_page = [&](int j, int bid) {
+      if (bid >= p.num_blocks) {
+        flag_status(p.status, PKV_STATUS_BAD_BLOCK);
+        bid = 0;
+      }
+      tma_load_2d(stage + j * kStagePage, map, 0, (bid * p.Hkv + g) * kPage, bar_st);
+      bulk_copy(ssc + j * kScaleBytes, scl + (size_t(bid) * p.Hkv + g) * kScaleBytes, kScaleBytes, bar_st);
+    };
+    if constexpr (F8) {
+      int ids0[kPfPagesPerTile];
+#pragma unroll
+      for (int j = 0; j < kPfPagesPerTile; ++j) ids0[j] = __shfl_sync(0xffffffffu, cur_g, j);
+      if (lane == 0) {
+        arm_stage(ids0);
+        for (int j = 0; j < kPfPagesPerTile; ++j)
+          if (ids0[j] >= 0) stage_page(j, ids0[j]);
+      }
+      st_pending = 0;
+    }
     for (int kt = 0; kt < nkv; ++kt) {
       if (kt > 0 && (kt & 3) == 0) {
         cur_g = next_g;  // read four tiles ago
@@ -429,13 +529,53 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         ok = false;
         break;
       }
-      if (lane == 0) load_tile(map, base0 + kb * 2 * kHalfTile, bar_load + kb, ids);
+      if constexpr (!F8) {
+        if (lane == 0) load_tile(map, base0 + kb * 2 * kHalfTile, bar_load + kb, ids);
+      } else {
+        // block ids of the next tile: its staging copies go out page by page
+        // as this tile's pages are widened
+        const int kn = kt + 1;
+        const int src_g = (kn & 3) == 0 ? next_g : cur_g;
+        int nids[kPfPagesPerTile];
+#pragma unroll
+        for (int j = 0; j < kPfPagesPerTile; ++j) {
+          const int v = __shfl_sync(0xffffffffu, src_g, (kn & 3) * 8 + j);
+          nids[j] = kn < nkv ? v : -1;
+        }
+        // every lane reads the staged bytes, so every lane waits
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_st, kt & 1))) {
+          ok = false;
+          break;
+        }
+        st_pending = -1;
+        if (kn < nkv) {
+          if (lane == 0) arm_stage(nids);
+          st_pending = kn;
+        }
+        uint8_t* dst = base0 + kb * 2 * kHalfTile;
+        const int r = lane >> 1, h = lane & 1;
+#pragma unroll
+        for (int j = 0; j < kPfPagesPerTile; ++j) {
+          if (ids[j] >= 0)
+            widen_row_half(stage + j * kStagePage, ssc[j * kScaleBytes + r],
+                           dst + h * kHalfTile + (j * kPage + r) * 128, r, h);
+          __syncwarp();
+          if (lane == 0 && nids[j] >= 0) {
+            fence_proxy_async_smem();  // the slot's reads are done before the copy rewrites it
+            stage_page(j, nids[j]);
+          }
+        }
+        fence_proxy_async_smem();  // widened rows -> visible to the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_load + kb);
+      }
       ++loaded;
     }
     if (lane == 0) {
       // copies land before the CTA's shared memory is released
       for (int k = max(0, loaded - kKVBufs); k < loaded; ++k)
         mbar_wait(bar_load + k % kKVBufs, (k / kKVBufs) & 1, ok ? kWaitLimitNs : kDrainLimitNs);
+      if (F8 && st_pending >= 0) mbar_wait(bar_st, st_pending & 1, ok ? kWaitLimitNs : kDrainLimitNs);
       if (!ok) flag_status(p.status, PKV_STATUS_TIMEOUT);
     }
     __syncwarp();
@@ -510,7 +650,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     // running max (same in both threads of a row) and half row sum, per tile
     float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
-    float* s_red = reinterpret_cast<float*>(sm + kOffMisc + 256);  // [2][128] exchange
+    float* s_red = reinterpret_cast<float*>(sm + kOffM + 256);  // [2][128] exchange
     bool ok = true;
     for (int it = 0; it < nkv && ok; ++it) {
       for (int u = 0; u < nt; ++u) {
@@ -749,17 +889,17 @@ int prefill_max_tiles(const pkv_desc& d, int32_t num_seqs, int32_t num_tokens) {
   return (num_tokens + tm - 1) / tm + num_seqs;
 }
 
-template <bool PREFIX>
+template <bool PREFIX, bool F8>
 static int ensure_prefill_attr(int device) {
-  static bool done[2][64] = {};
+  static bool done[64] = {};
   if (device < 0 || device >= 64) return PKV_ERR_DEVICE;
-  if (!done[PREFIX][device]) {
-    if (cudaFuncSetAttribute(pkv_prefill_kernel<PREFIX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kPfSmemBytes)) != cudaSuccess) {
+  if (!done[device]) {
+    if (cudaFuncSetAttribute(pkv_prefill_kernel<PREFIX, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kPfSmemOf<F8>)) != cudaSuccess) {
       cudaGetLastError();
       return PKV_ERR_LAUNCH;
     }
-    done[PREFIX][device] = true;
+    done[device] = true;
   }
   return PKV_OK;
 }
@@ -774,6 +914,16 @@ static int make_maps(const AttendArgs& a, CUtensorMap* tq, CUtensorMap* tk, CUte
     if (!encode(tq, a.q, 3, dims, strides, box)) return PKV_ERR_LAUNCH;
   }
   const cuuint64_t rows = cuuint64_t(d.num_blocks) * d.num_kv_heads * kPage;
+  if (a.fp8) {
+    // E4M3 codes as [rows][128]: one box = one page of 16 rows
+    const cuuint64_t dims[2] = {cuuint64_t(kHeadDim), rows};
+    const cuuint64_t strides[1] = {cuuint64_t(kHeadDim)};
+    const cuuint32_t box[2] = {cuuint32_t(kHeadDim), cuuint32_t(kPage)};
+    if (!encode_tensor_map(tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.k_cache, 2, dims, strides, box) ||
+        !encode_tensor_map(tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.v_cache, 2, dims, strides, box))
+      return PKV_ERR_LAUNCH;
+    return PKV_OK;
+  }
   const cuuint64_t dims[2] = {cuuint64_t(kHeadDim), rows};
   const cuuint64_t strides[1] = {cuuint64_t(kHeadDim) * 2};
   const cuuint32_t box[2] = {64, cuuint32_t(kPage)};
@@ -800,12 +950,16 @@ static PrefillParams make_params(const LaunchCtx& ctx, const AttendArgs& a, int 
   pp.num_blocks = d.num_blocks;
   pp.split_max_q = split_max_q;
   pp.qscale = a.scale * 1.4426950408889634f;
+  pp.k_scale = a.k_scale;
+  pp.v_scale = a.v_scale;
   return pp;
 }
 
 int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, void* /*scratch*/, int split_max_q,
                    int max_tiles) {
-  if (int e = ensure_prefill_attr<false>(ctx.dev->device)) return e;
+  if (int e = a.fp8 ? ensure_prefill_attr<false, true>(ctx.dev->device)
+                    : ensure_prefill_attr<false, false>(ctx.dev->device))
+    return e;
   CUtensorMap tq, tk, tv;
   if (int e = make_maps(a, &tq, &tk, &tv)) return e;
   const PrefillParams pp = make_params(ctx, a, split_max_q);
@@ -813,8 +967,12 @@ int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, void* /*scratch*/,
   const int tg = 2 * pp.TM;
   const int groups = min(max_tiles, (a.num_tokens + tg - 1) / tg + a.num_seqs);
   TraceScope ts(ctx.stream, PKV_K_PREFILL);
-  pkv_prefill_kernel<false><<<dim3(a.desc.num_kv_heads, groups), kPfThreads, kPfSmemBytes,
-                              ctx.stream>>>(tq, tk, tv, pp);
+  if (a.fp8)
+    pkv_prefill_kernel<false, true><<<dim3(a.desc.num_kv_heads, groups), kPfThreads, kPfSmemOf<true>,
+                                      ctx.stream>>>(tq, tk, tv, pp);
+  else
+    pkv_prefill_kernel<false, false><<<dim3(a.desc.num_kv_heads, groups), kPfThreads, kPfSmemOf<false>,
+                                       ctx.stream>>>(tq, tk, tv, pp);
   return ts.done();
 }
 
@@ -836,7 +994,7 @@ int prefix_chunks(const pkv_desc& d, int32_t num_tokens, int32_t prefix_pages, i
 
 int launch_prefix(const LaunchCtx& ctx, const AttendArgs& a, float* records, int chunks,
                   int chunk_tiles) {
-  if (int e = ensure_prefill_attr<true>(ctx.dev->device)) return e;
+  if (int e = ensure_prefill_attr<true, false>(ctx.dev->device)) return e;
   CUtensorMap tq, tk, tv;
   if (int e = make_maps(a, &tq, &tk, &tv)) return e;
   PrefillParams pp = make_params(ctx, a, 0);
@@ -846,7 +1004,7 @@ int launch_prefix(const LaunchCtx& ctx, const AttendArgs& a, float* records, int
   pp.prefix_part = records;
   const int qgroups = (a.num_tokens + pp.TM - 1) / pp.TM;
   TraceScope ts(ctx.stream, PKV_K_PREFILL);
-  pkv_prefill_kernel<true><<<dim3(a.desc.num_kv_heads, qgroups * chunks), kPfThreads, kPfSmemBytes,
+  pkv_prefill_kernel<true, false><<<dim3(a.desc.num_kv_heads, qgroups * chunks), kPfThreads, kPfSmemOf<false>,
                              ctx.stream>>>(tq, tk, tv, pp);
   return ts.done();
 }

@@ -128,7 +128,8 @@ def test_attend_fp8_long_tail_sampled_rows(pkvlib):
 
 
 def test_attend_fp8_mixed_step_sampled_rows(pkvlib):
-    """Prefill chunks of 512 rows run through split-KV on FP8 pages."""
+    """Prefill chunks of 512 rows on the tensor-core kernel, decode rows on
+    split-KV, FP8 pages."""
     b = workload(5, device="cuda")
     rng = np.random.default_rng(5)
     rows = sorted(set([96, 97, 300, 96 + 511, 96 + 512, 96 + 1023] + rng.choice(96, 6, replace=False).tolist()))
@@ -167,6 +168,45 @@ def test_attend_fp8_stale_rows_do_not_leak(pkvlib):
     expected = O.attend_fp8(bits(b.q), *ref, b.block_tables, b.seq_lens, b.query_start_loc, b.scale,
                             b.num_q_heads, b.num_kv_heads, b.page_size)
     compare(out, expected, what="fp8 stale")
+
+
+@pytest.mark.parametrize("hq,hkv,L,n", [(32, 8, 1100, 130), (16, 2, 257, 257), (8, 8, 640, 300),
+                                        (32, 2, 129, 33), (64, 4, 3000, 17), (32, 8, 2000, 100)])
+def test_attend_fp8_prefill_chunks_all_rows(pkvlib, hq, hkv, L, n):
+    """Chunks longer than the split-KV bound run on the tensor-core kernel, the
+    pages widened exactly to bf16 in shared memory; every row."""
+    b = make_batch([L, 40], [n, 1], hq, hkv, seed=L + n + 7, device="cuda")
+    tr = pkv.Trace(64)
+    with tr:
+        _run(b, L + n, what=f"fp8 prefill {hq}/{hkv} L={L} n={n}")
+    counts = {k: tr.read(k)[1] for k in ("decode", "prefill")}
+    tr.close()
+    assert counts["prefill"] == 1
+
+
+def test_attend_fp8_prefill_stale_rows_do_not_leak(pkvlib):
+    """A prefill chunk whose last page is partly past the sequence: those rows
+    hold NaN codes and scale bytes 0 and 255, and must not reach the output."""
+    b = make_batch([17, 150, 250], [1, 40, 1], 8, 2, seed=33, device="cuda")
+    kc, vc, ks, vs = fp8_pools(b, 34)
+    for bi in range(b.B):
+        L = int(b.seq_lens[bi])
+        last = int(b.block_tables[bi, (L - 1) // 16])
+        if L % 16:
+            kc[last, :, L % 16:, :] = 0x7F
+            vc[last, :, L % 16:, :] = 0xFF
+            ks[last, :, L % 16:] = 255
+            vs[last, :, L % 16:] = 0
+    pools = (kc, vc, ks, vs)
+    meta = to_device(b)
+    g = _gpu_write(b, pools, meta)
+    out = pkv.attend_fp8(b.q, *g, meta["block_tables"], meta["seq_lens"], meta["query_start_loc"], b.scale)
+    torch.cuda.synchronize()
+    assert pkv.get_last_error() == 0
+    ref = _oracle_write(b, pools)
+    expected = O.attend_fp8(bits(b.q), *ref, b.block_tables, b.seq_lens, b.query_start_loc, b.scale,
+                            b.num_q_heads, b.num_kv_heads, b.page_size)
+    compare(out, expected, what="fp8 prefill stale")
 
 
 def test_attend_fp8_close_to_bf16_attention_of_the_same_rows(pkvlib):
@@ -208,13 +248,13 @@ def test_attend_fp8_rejects_bad_arguments(pkvlib):
     import ctypes
     P = pkv._ptr
     args = lambda ksp: (P(b.q), P(kc), P(vc), ksp, P(vs), P(meta["block_tables"]), P(meta["seq_lens"]),
-                        P(meta["query_start_loc"]), b.B, b.T, ctypes.c_float(b.scale), P(out), P(ws),
+                        P(meta["query_start_loc"]), b.B, b.T, 0, ctypes.c_float(b.scale), P(out), P(ws),
                         ws.numel(), ctypes.byref(desc), pkv._stream(b.q.device, None))
     assert lib.pkv_attend_fp8(*args(ctypes.c_void_p(0))) == -1          # PKV_ERR_NULL
     assert lib.pkv_attend_fp8(*args(ctypes.c_void_p(ks.data_ptr() + 1))) == -2  # PKV_ERR_ALIGN
     assert lib.pkv_attend_fp8(*args(P(ks))) == 0
     short = ctypes.c_size_t(ws.numel() - 256)
     a = list(args(P(ks)))
-    a[13] = short
+    a[14] = short
     assert lib.pkv_attend_fp8(*a) == -5  # PKV_ERR_WORKSPACE
     torch.cuda.synchronize()
