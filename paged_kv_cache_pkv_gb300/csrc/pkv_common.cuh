@@ -138,6 +138,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   return true;
 }
 
+// mbar_wait that sleeps `sleep_ns` between tests once the first test failed:
+// for warps whose wait is long and off the critical path, so that they leave
+// their sub-partition's issue slots to a warp doing arithmetic.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, uint32_t sleep_ns,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+
+
 // L2 policy for data read exactly once (KV pages of a decode step).
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;

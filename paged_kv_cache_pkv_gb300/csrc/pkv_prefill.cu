@@ -255,28 +255,77 @@ __device__ __forceinline__ uint32_t widen_pair(uint32_t h2, float sc) {
   return pack_bf16x2(f.x * sc, f.y * sc);
 }
 
+// Four E4M3 codes (lowest byte first) times 2^(scale-127) -> four bf16 (two
+// pairs, lowest first), integer arithmetic only.  For a code with a nonzero
+// exponent field E and mantissa m, the product is 2^(E-7) * (1 + m/8) *
+// 2^(scale-127): bf16 exponent field E + scale - 7, mantissa m in its top
+// three bits, the sign as is.  `adj` is (scale - 7) << 7 in both halves; it
+// is exact for scale in [7, 246] (exponent fields 1..254) and codes with a
+// nonzero exponent field (zero and subnormal codes take the f16 route).
+__device__ __forceinline__ void widen4_int(uint32_t w, uint32_t adj, uint32_t& lo, uint32_t& hi) {
+  const uint32_t p0 = __byte_perm(w, 0u, 0x1404u);  // codes 0, 1 in the high byte of each half
+  const uint32_t p1 = __byte_perm(w, 0u, 0x3424u);  // codes 2, 3
+  lo = (((p0 >> 4) & 0x07F007F0u) + adj) | (p0 & 0x80008000u);
+  hi = (((p1 >> 4) & 0x07F007F0u) + adj) | (p1 & 0x80008000u);
+}
+
+// Nonzero when some code of w has a zero exponent field (zero or subnormal).
+__device__ __forceinline__ uint32_t zero_field(uint32_t w) {
+  const uint32_t t = w & 0x78787878u;
+  return (t - 0x01010101u) & ~t & 0x80808080u;
+}
+
+// Same through f16 (exact for every finite code and any scale byte).
+__device__ __forceinline__ void widen4_f16(uint32_t w, float sc, uint32_t& lo, uint32_t& hi) {
+  uint32_t a0, a1;
+  e4m3x4_f16x2(w, a0, a1);
+  lo = widen_pair(a0, sc);
+  hi = widen_pair(a1, sc);
+}
+
 // One lane's half row of an FP8 page: codes of dims 64h..64h+63 of row r (the
 // staged page as TMA laid it out, 128-byte swizzle) times 2^(scale-127), as
 // bf16 into row `drow` of the half-h block of a K/V tile (128-byte swizzle,
 // row index = key within the tile, congruent to r mod 8).  The chunk order
 // c = cc ^ 4h keeps each quarter-warp's 16-byte stores on distinct banks.
+// One branch per lane: the integer route when the scale byte and every code
+// allow it (nearly always), else the f16 route.  Words are picked with
+// compile-time indices (a select on h), so w[] stays in registers.
 __device__ __forceinline__ void widen_row_half(const uint8_t* spage, uint32_t sbyte, uint8_t* drow,
                                                int r, int h) {
-  uint4 c4[4];
+  uint32_t w[16];  // codes of dims 64h + 4k .. 64h + 4k + 3
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    c4[i] = *reinterpret_cast<const uint4*>(spage + r * 128 + (((4 * h + i) ^ (r & 7)) << 4));
-  const float sc = __uint_as_float(sbyte << 23);  // 2^(sbyte-127); byte 0 is never written
+  for (int i = 0; i < 4; ++i) {
+    const uint4 v = *reinterpret_cast<const uint4*>(spage + r * 128 + (((4 * h + i) ^ (r & 7)) << 4));
+    w[4 * i] = v.x;
+    w[4 * i + 1] = v.y;
+    w[4 * i + 2] = v.z;
+    w[4 * i + 3] = v.w;
+  }
+  uint32_t z = 0;
 #pragma unroll
-  for (int cc = 0; cc < 8; ++cc) {
-    const int c = cc ^ (h << 2);  // dims 8c..8c+7 of the half
-    const uint4 src = c4[c >> 1];
-    const uint32_t w0 = (c & 1) ? src.z : src.x, w1 = (c & 1) ? src.w : src.y;
-    uint32_t a0, a1, a2, a3;
-    e4m3x4_f16x2(w0, a0, a1);
-    e4m3x4_f16x2(w1, a2, a3);
-    const uint4 o = make_uint4(widen_pair(a0, sc), widen_pair(a1, sc), widen_pair(a2, sc), widen_pair(a3, sc));
-    *reinterpret_cast<uint4*>(drow + ((c ^ (r & 7)) << 4)) = o;
+  for (int k = 0; k < 16; ++k) z |= zero_field(w[k]);
+  if (z == 0u && sbyte >= 7u && sbyte <= 246u) {
+    const uint32_t adj = ((sbyte - 7u) << 7) * 0x00010001u;
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+      const int c = cc ^ (h << 2);  // dims 8c..8c+7 of the half
+      const uint32_t wa = h ? w[2 * (cc ^ 4)] : w[2 * cc];
+      const uint32_t wb = h ? w[2 * (cc ^ 4) + 1] : w[2 * cc + 1];
+      uint4 o;
+      widen4_int(wa, adj, o.x, o.y);
+      widen4_int(wb, adj, o.z, o.w);
+      *reinterpret_cast<uint4*>(drow + ((c ^ (r & 7)) << 4)) = o;
+    }
+  } else {
+    const float sc = __uint_as_float(sbyte << 23);  // 2^(sbyte-127); byte 0 is never written
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint4 o;
+      widen4_f16(w[2 * c], sc, o.x, o.y);
+      widen4_f16(w[2 * c + 1], sc, o.z, o.w);
+      *reinterpret_cast<uint4*>(drow + ((c ^ (r & 7)) << 4)) = o;
+    }
   }
 }
 
@@ -433,6 +482,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t idesc_s = idesc_bf16(128, 128, false);
   const uint32_t idesc_o = idesc_bf16(128, 128, true);
   const int role = warp - kPfSoftmaxThreads / 32;  // 0: K loads, 1: V loads, 2 + u: MMA of Q tile u; < 0 softmax
+  // With FP8 pages the loader warps widen every tile and set the pace; the
+  // softmax and MMA warps, which share their sub-partitions, sleep between
+  // barrier tests instead of spinning.
+  auto wait_idle = [&](uint64_t* bar, uint32_t parity) {
+    return F8 ? mbar_wait_backoff(bar, parity, 256) : mbar_wait(bar, parity);
+  };
 
   auto load_tile = [&](const CUtensorMap* map, uint8_t* base, uint64_t* bar, const int (&bids)[kPfPagesPerTile]) {
     int valid = 0;
@@ -559,11 +614,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (ids[j] >= 0)
             widen_row_half(stage + j * kStagePage, ssc[j * kScaleBytes + r],
                            dst + h * kHalfTile + (j * kPage + r) * 128, r, h);
-          __syncwarp();
-          if (lane == 0 && nids[j] >= 0) {
-            fence_proxy_async_smem();  // the slot's reads are done before the copy rewrites it
-            stage_page(j, nids[j]);
-          }
+          __syncwarp();  // every lane has consumed the slot's codes: the copy may rewrite it
+          if (lane == 0 && nids[j] >= 0) stage_page(j, nids[j]);
         }
         fence_proxy_async_smem();  // widened rows -> visible to the tensor cores
         __syncwarp();
@@ -601,7 +653,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         umma_commit(bar_kfree + kb * 2 + u);
       };
       int ns = 0, npv = 0;  // S and PV groups issued (for the drain on failure)
-      bool ok = mbar_wait(bar_q, 0) && mbar_wait(bar_k, 0);
+      bool ok = wait_idle(bar_q, 0) && wait_idle(bar_k, 0);
       if (ok) {
         issue_s(0);
         ++ns;
@@ -609,7 +661,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int it = 0; ok && it < nkv; ++it) {
         const int vb = it % kKVBufs;
         // P(u, it) written by the softmax; V(it) landed
-        if (!(ok = mbar_wait(bar_p + u, it & 1) && mbar_wait(bar_v + vb, (it / kKVBufs) & 1))) break;
+        if (!(ok = wait_idle(bar_p + u, it & 1) && wait_idle(bar_v + vb, (it / kKVBufs) & 1))) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {  // 16 keys = 8 packed TMEM columns of P
@@ -621,7 +673,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         umma_commit(bar_vfree + vb * 2 + u);
         ++npv;
         if (it + 1 < nkv) {
-          if (!(ok = mbar_wait(bar_k + (it + 1) % kKVBufs, ((it + 1) / kKVBufs) & 1))) break;
+          if (!(ok = wait_idle(bar_k + (it + 1) % kKVBufs, ((it + 1) / kKVBufs) & 1))) break;
           issue_s(it + 1);
           ++ns;
         }
@@ -657,7 +709,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int ph = it & 1;
         const int posu = u ? pos[1] : pos[0];
         float m = u ? m1 : m0;
-        ok = mbar_wait(bar_s + u, ph) && ok;
+        ok = wait_idle(bar_s + u, ph) && ok;
         tc_fence_after();
         // ---- this thread's 64 columns of row r ----
         const int kbase = (kbeg + it) * kPfKeys + ch * 64;
