@@ -588,15 +588,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (lane == 0) load_tile(map, base0 + kb * 2 * kHalfTile, bar_load + kb, ids);
       } else {
         // block ids of the next tile: its staging copies go out page by page
-        // as this tile's pages are widened
+        // as this tile's pages are widened.  Ids come by shuffle inside the
+        // (rolled) page loop, which keeps this role's code small.
         const int kn = kt + 1;
         const int src_g = (kn & 3) == 0 ? next_g : cur_g;
-        int nids[kPfPagesPerTile];
-#pragma unroll
-        for (int j = 0; j < kPfPagesPerTile; ++j) {
-          const int v = __shfl_sync(0xffffffffu, src_g, (kn & 3) * 8 + j);
-          nids[j] = kn < nkv ? v : -1;
-        }
+        const int cur_lane0 = (kt & 3) * 8, nxt_lane0 = (kn & 3) * 8;
+        const uint32_t nvalid_mask = __ballot_sync(0xffffffffu, src_g >= 0);
         // every lane reads the staged bytes, so every lane waits
         if (!__all_sync(0xffffffffu, mbar_wait(bar_st, kt & 1))) {
           ok = false;
@@ -604,18 +601,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         st_pending = -1;
         if (kn < nkv) {
-          if (lane == 0) arm_stage(nids);
+          if (lane == 0) {
+            const int valid = __popc((nvalid_mask >> nxt_lane0) & 0xFFu);
+            mbar_arrive_expect_tx(bar_st, uint32_t(valid) * (kStagePage + kScaleBytes));
+          }
           st_pending = kn;
         }
         uint8_t* dst = base0 + kb * 2 * kHalfTile;
         const int r = lane >> 1, h = lane & 1;
-#pragma unroll
+#pragma unroll 1
         for (int j = 0; j < kPfPagesPerTile; ++j) {
-          if (ids[j] >= 0)
+          const int idj = __shfl_sync(0xffffffffu, cur_g, cur_lane0 + j);
+          const int nidj = __shfl_sync(0xffffffffu, src_g, nxt_lane0 + j);
+          if (idj >= 0)
             widen_row_half(stage + j * kStagePage, ssc[j * kScaleBytes + r],
                            dst + h * kHalfTile + (j * kPage + r) * 128, r, h);
           __syncwarp();  // every lane has consumed the slot's codes: the copy may rewrite it
-          if (lane == 0 && nids[j] >= 0) stage_page(j, nids[j]);
+          if (lane == 0 && kn < nkv && nidj >= 0) stage_page(j, nidj);
         }
         fence_proxy_async_smem();  // widened rows -> visible to the tensor cores
         __syncwarp();
