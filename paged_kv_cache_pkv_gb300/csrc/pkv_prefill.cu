@@ -775,8 +775,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // redo the pass against the new maximum; warp-uniform (TMEM loads are
         // warp-collective), rows whose maximum did not move recompute the same P
         if (warp_grow) {
-          if (full) pass(m, std::true_type{}, std::false_type{});
-          else pass(m, std::false_type{}, std::false_type{});
+          // (the tracking variant again: one copy of the pass code less, and
+          // its maximum is not used after the exchange)
+          if (full) pass(m, std::true_type{}, std::true_type{});
+          else pass(m, std::false_type{}, std::true_type{});
         }
         if (u) {
           m1 = m;
