@@ -254,7 +254,7 @@ def main():
         kc, vc = b.k_cache, b.v_cache
     out = torch.empty_like(b.q)
     desc = pkv.make_desc(kc, b.num_q_heads, bt.shape[1])
-    ws_bytes = (pkv.workspace_size_fp8(desc, b.B, b.T, dev) if fp8 else
+    ws_bytes = (pkv.workspace_size_fp8(desc, b.B, b.T, dev, int(b.info.get("shared_prefix_pages", 0))) if fp8 else
                 pkv.workspace_size(desc, b.B, b.T, dev, int(b.info.get("shared_prefix_pages", 0))))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     # L2 flush before every step: write 256 MiB, then read another 256 MiB, so
@@ -272,14 +272,12 @@ def main():
     max_q = int(b.q_lens.max())  # the scheduler knows its largest query chunk
     prefix = int(b.info.get("shared_prefix_pages", 0))  # and the prefix its sequences share
 
-    if fp8 and prefix:
-        raise SystemExit("FP8 pages have no shared-prefix cascade; pick another workload")
 
     def step():
         if fp8:
             pkv.write_fp8(b.k_new, b.v_new, slots, kc, vc, ks, vs)
             pkv.attend_fp8(b.q, kc, vc, ks, vs, bt, lens, qsl, b.scale, out=out, workspace=ws,
-                           max_query_len=max_q)
+                           max_query_len=max_q, shared_prefix_pages=prefix)
             return
         pkv.write(b.k_new, b.v_new, slots, kc, vc)
         pkv.attend(b.q, kc, vc, bt, lens, qsl, b.scale, out=out, workspace=ws, max_query_len=max_q,
@@ -377,7 +375,7 @@ def main():
         if fp8:
             pkv.write_fp8(dev_in["k_new"], dev_in["v_new"], dev_in["slots"], kc, vc, ks, vs)
             pkv.attend_fp8(dev_in["q"], kc, vc, ks, vs, dev_in["bt"], dev_in["lens"], dev_in["qsl"],
-                           b.scale, out=out, workspace=ws, max_query_len=max_q)
+                           b.scale, out=out, workspace=ws, max_query_len=max_q, shared_prefix_pages=prefix)
         else:
             pkv.write(dev_in["k_new"], dev_in["v_new"], dev_in["slots"], kc, vc)
             pkv.attend(dev_in["q"], kc, vc, dev_in["bt"], dev_in["lens"], dev_in["qsl"], b.scale, out=out,

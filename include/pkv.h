@@ -236,18 +236,21 @@ PKV_API int pkv_write_fp8(const pkv_bf16* k_new, const pkv_bf16* v_new,
                           uint8_t* v_scale, const pkv_desc* desc, pkv_stream_t stream);
 
 /* Workspace bytes pkv_attend_fp8 needs on the CURRENT device (its kernel
- * runs a different number of warps than pkv_attend's).  Writes *bytes. */
+ * runs a different number of warps than pkv_attend's), for num_seqs
+ * sequences, num_tokens query rows and shared_prefix_pages as passed to
+ * pkv_attend_fp8.  Writes *bytes. */
 PKV_API int pkv_attend_fp8_workspace_size(const pkv_desc* desc, int32_t num_seqs,
-                                          int32_t num_tokens, size_t* bytes);
+                                          int32_t num_tokens, int32_t shared_prefix_pages,
+                                          size_t* bytes);
 
 /* pkv_attend_fp8 -- pkv_attend over FP8 pages: the same result with K and V
  * the exact values code * 2^(scale - 127).  Query chunks longer than
  * PKV_SPLITKV_MAX_QLEN run on the tensor-core prefill kernel (the pages
  * widened exactly to bf16 in shared memory), the rest on split-KV, as in
- * pkv_attend; max_query_len has pkv_attend's meaning.  No shared-prefix
- * cascade for FP8 pages.  workspace: at least
- * pkv_attend_fp8_workspace_size(desc, num_seqs, num_tokens) bytes, 256-byte
- * aligned, no initialisation needed.  Scale bytes of rows a query sees must
+ * pkv_attend; max_query_len and shared_prefix_pages (the cascade over a
+ * prefix every sequence shares) have pkv_attend's meaning.  workspace: at
+ * least pkv_attend_fp8_workspace_size(desc, num_seqs, num_tokens,
+ * shared_prefix_pages) bytes, 256-byte aligned, no initialisation needed.  Scale bytes of rows a query sees must
  * lie in [1, 254] (pkv_write_fp8 writes nothing else); rows it does not see
  * are never used, whatever they hold. */
 PKV_API int pkv_attend_fp8(const pkv_bf16* q, const pkv_fp8* k_cache,
@@ -255,7 +258,7 @@ PKV_API int pkv_attend_fp8(const pkv_bf16* q, const pkv_fp8* k_cache,
                            const uint8_t* v_scale, const int32_t* block_tables,
                            const int32_t* seq_lens, const int32_t* query_start_loc,
                            int32_t num_seqs, int32_t num_tokens, int32_t max_query_len,
-                           float scale,
+                           int32_t shared_prefix_pages, float scale,
                            pkv_bf16* out, void* workspace, size_t workspace_bytes,
                            const pkv_desc* desc, pkv_stream_t stream);
 

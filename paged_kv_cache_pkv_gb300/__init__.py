@@ -57,8 +57,8 @@ _SIGS = {
     "pkv_attend_static": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                          ctypes.c_float, _vp, ctypes.POINTER(Desc), _vp]),
     "pkv_write_fp8": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, ctypes.POINTER(Desc), _vp]),
-    "pkv_attend_fp8_workspace_size": (ctypes.c_int, [ctypes.POINTER(Desc), _i32, _i32, ctypes.POINTER(_sz)]),
-    "pkv_attend_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_float,
+    "pkv_attend_fp8_workspace_size": (ctypes.c_int, [ctypes.POINTER(Desc), _i32, _i32, _i32, ctypes.POINTER(_sz)]),
+    "pkv_attend_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, ctypes.c_float,
                                       _vp, _vp, _sz, ctypes.POINTER(Desc), _vp]),
     "pkv_get_last_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
     "pkv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -236,20 +236,21 @@ def write_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, st
                "pkv_write_fp8")
 
 
-def workspace_size_fp8(desc, num_seqs, num_tokens, device=None):
+def workspace_size_fp8(desc, num_seqs, num_tokens, device=None, shared_prefix_pages=0):
     """Workspace bytes attend_fp8 needs for a batch of this size."""
     n = _sz(0)
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
         _check(lib().pkv_attend_fp8_workspace_size(ctypes.byref(desc), int(num_seqs), int(num_tokens),
-                                                   ctypes.byref(n)), "pkv_attend_fp8_workspace_size")
+                                                   int(shared_prefix_pages), ctypes.byref(n)),
+               "pkv_attend_fp8_workspace_size")
     return n.value
 
 
 def attend_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, query_start_loc, scale,
-               out=None, workspace=None, stream=None, max_query_len=0):
+               out=None, workspace=None, stream=None, max_query_len=0, shared_prefix_pages=0):
     """attend() over FP8 pages (codes and per-row scale bytes as written by
     write_fp8): long query chunks on the tensor-core prefill kernel, the rest
-    on split-KV; max_query_len as in attend() (0: unknown)."""
+    on split-KV; max_query_len and shared_prefix_pages as in attend()."""
     _need(q, "q", torch.bfloat16, 3)
     _need_fp8_pool(k_cache, v_cache, k_scale, v_scale)
     _need(block_tables, "block_tables", torch.int32, 2)
@@ -268,7 +269,7 @@ def attend_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, qu
         _need(out, "out", torch.bfloat16, 3)
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
-    need = workspace_size_fp8(desc, B, T, q.device)
+    need = workspace_size_fp8(desc, B, T, q.device, shared_prefix_pages)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     else:
@@ -278,9 +279,9 @@ def attend_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, qu
     with torch.cuda.device(q.device):
         _check(lib().pkv_attend_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                     _ptr(block_tables), _ptr(seq_lens), _ptr(query_start_loc), B, T,
-                                    int(max_query_len), float(scale), _ptr(out), _ptr(workspace),
-                                    workspace.numel(),
-                                    ctypes.byref(desc), _stream(q.device, stream)),
+                                    int(max_query_len), int(shared_prefix_pages), float(scale), _ptr(out),
+                                    _ptr(workspace), workspace.numel(), ctypes.byref(desc),
+                                    _stream(q.device, stream)),
                "pkv_attend_fp8")
     return out
 

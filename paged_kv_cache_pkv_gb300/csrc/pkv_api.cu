@@ -175,14 +175,14 @@ int pkv_attend_workspace_size(const pkv_desc* desc, int32_t num_seqs, int32_t nu
 }
 
 int pkv_attend_fp8_workspace_size(const pkv_desc* desc, int32_t num_seqs, int32_t num_tokens,
-                                  size_t* bytes) {
+                                  int32_t shared_prefix_pages, size_t* bytes) {
   if (int e = check_desc(desc)) return e;
   if (!bytes) return PKV_ERR_NULL;
-  if (num_seqs < 0 || num_tokens < 0) return PKV_ERR_RANGE;
+  if (num_seqs < 0 || num_tokens < 0 || shared_prefix_pages < 0) return PKV_ERR_RANGE;
   int err = PKV_OK;
   const DeviceInfo* dev = current_device(&err);
   if (!dev) return err;
-  *bytes = attend_workspace_bytes(*dev, *desc, num_seqs, num_tokens, 0, true);
+  *bytes = attend_workspace_bytes(*dev, *desc, num_seqs, num_tokens, shared_prefix_pages, true);
   return PKV_OK;
 }
 
@@ -230,7 +230,8 @@ int pkv_write_fp8(const pkv_bf16* k_new, const pkv_bf16* v_new, const int64_t* s
 int pkv_attend_fp8(const pkv_bf16* q, const pkv_fp8* k_cache, const pkv_fp8* v_cache,
                    const uint8_t* k_scale, const uint8_t* v_scale, const int32_t* block_tables,
                    const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_seqs,
-                   int32_t num_tokens, int32_t max_query_len, float scale, pkv_bf16* out,
+                   int32_t num_tokens, int32_t max_query_len, int32_t shared_prefix_pages,
+                   float scale, pkv_bf16* out,
                    void* workspace, size_t workspace_bytes, const pkv_desc* desc,
                    pkv_stream_t stream) {
   if (int e = check_desc(desc)) return e;
@@ -246,7 +247,8 @@ int pkv_attend_fp8(const pkv_bf16* q, const pkv_fp8* k_cache, const pkv_fp8* v_c
   LaunchCtx ctx;
   if (int e = make_ctx(stream, &ctx)) return e;
   AttendArgs a{q,     k_cache, v_cache,   block_tables,    seq_lens, query_start_loc,
-               num_seqs, num_tokens, max_query_len, 0, scale, out, workspace, workspace_bytes, *desc};
+               num_seqs, num_tokens, max_query_len, shared_prefix_pages, scale, out, workspace,
+               workspace_bytes, *desc};
   a.fp8 = true;
   a.k_scale = k_scale;
   a.v_scale = v_scale;

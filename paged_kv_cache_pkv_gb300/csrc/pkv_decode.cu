@@ -1176,7 +1176,6 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   const int nsub = G / GH;
   const int nwarps = a.fp8 ? ctx.dev->dec_warps_f8[variant_of(GH)] : ctx.dev->dec_warps[variant_of(GH)];
   if (nwarps <= 0) return PKV_ERR_LAUNCH;
-  if (a.fp8 && a.shared_prefix_pages != 0) return PKV_ERR_RANGE;
   if (a.num_seqs > kMaxSeqs) return PKV_ERR_RANGE;
   // unit indices are int32 on the device
   if (int64_t(a.num_tokens) * d.max_blocks_per_seq * d.num_kv_heads * nsub >= (int64_t(1) << 31))

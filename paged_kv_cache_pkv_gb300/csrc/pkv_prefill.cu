@@ -1050,7 +1050,9 @@ int prefix_chunks(const pkv_desc& d, int32_t num_tokens, int32_t prefix_pages, i
 
 int launch_prefix(const LaunchCtx& ctx, const AttendArgs& a, float* records, int chunks,
                   int chunk_tiles) {
-  if (int e = ensure_prefill_attr<true, false>(ctx.dev->device)) return e;
+  if (int e = a.fp8 ? ensure_prefill_attr<true, true>(ctx.dev->device)
+                    : ensure_prefill_attr<true, false>(ctx.dev->device))
+    return e;
   CUtensorMap tq, tk, tv;
   if (int e = make_maps(a, &tq, &tk, &tv)) return e;
   PrefillParams pp = make_params(ctx, a, 0);
@@ -1060,8 +1062,12 @@ int launch_prefix(const LaunchCtx& ctx, const AttendArgs& a, float* records, int
   pp.prefix_part = records;
   const int qgroups = (a.num_tokens + pp.TM - 1) / pp.TM;
   TraceScope ts(ctx.stream, PKV_K_PREFILL);
-  pkv_prefill_kernel<true, false><<<dim3(a.desc.num_kv_heads, qgroups * chunks), kPfThreads, kPfSmemOf<false>,
-                             ctx.stream>>>(tq, tk, tv, pp);
+  if (a.fp8)
+    pkv_prefill_kernel<true, true><<<dim3(a.desc.num_kv_heads, qgroups * chunks), kPfThreads,
+                                     kPfSmemOf<true>, ctx.stream>>>(tq, tk, tv, pp);
+  else
+    pkv_prefill_kernel<true, false><<<dim3(a.desc.num_kv_heads, qgroups * chunks), kPfThreads,
+                                      kPfSmemOf<false>, ctx.stream>>>(tq, tk, tv, pp);
   return ts.done();
 }
 

@@ -209,6 +209,55 @@ def test_attend_fp8_prefill_stale_rows_do_not_leak(pkvlib):
     compare(out, expected, what="fp8 prefill stale")
 
 
+def _cascade_fp8(batch, prefix_pages, seed, max_query_len=0, rows=None):
+    pools = fp8_pools(batch, seed)
+    meta = to_device(batch)
+    kc, vc, ks, vs = _gpu_write(batch, pools, meta)
+    out = pkv.attend_fp8(batch.q, kc, vc, ks, vs, meta["block_tables"], meta["seq_lens"],
+                         meta["query_start_loc"], batch.scale, max_query_len=max_query_len,
+                         shared_prefix_pages=prefix_pages)
+    torch.cuda.synchronize()
+    assert pkv.get_last_error() == 0
+    ref = _oracle_write(batch, pools)
+    expected = O.attend_fp8(bits(batch.q), *ref, batch.block_tables, batch.seq_lens,
+                            batch.query_start_loc, batch.scale, batch.num_q_heads,
+                            batch.num_kv_heads, batch.page_size, rows=rows)
+    return out, expected
+
+
+def test_attend_fp8_cascade_prefix_shared_workload(pkvlib):
+    """Config 4 on FP8 pages: 128 sequences on one 2048-token prefix, the
+    prefix attended once per kv head by the tensor-core prefix pass."""
+    b = workload(4, device="cuda")
+    rng = np.random.default_rng(4)
+    rows = sorted(rng.choice(b.T, 24, replace=False).tolist())
+    out, expected = _cascade_fp8(b, b.info["shared_prefix_pages"], 97, max_query_len=1, rows=rows)
+    compare(out, expected, rows=rows, what="fp8 cascade cfg4")
+
+
+@pytest.mark.parametrize("hq,hkv,prefix,suffixes", [
+    (32, 8, 80, [1, 17, 100, 16]),
+    (16, 2, 1600, [3, 250, 33]),
+    (64, 8, 512, [70, 5]),
+])
+def test_attend_fp8_cascade_small(pkvlib, hq, hkv, prefix, suffixes):
+    lens = [prefix + s for s in suffixes]
+    b = make_batch(lens, [1] * len(lens), hq, hkv, seed=prefix + 3, device="cuda",
+                   pool_factor=1.0, shared_prefix_tokens=prefix)
+    out, expected = _cascade_fp8(b, prefix // 16, prefix, max_query_len=1)
+    compare(out, expected, what=f"fp8 cascade {hq}/{hkv} prefix {prefix}")
+
+
+def test_attend_fp8_cascade_with_prefill_chunk(pkvlib):
+    """A shared prefix with decode rows, a short multi-row chunk (split-KV)
+    and a long chunk (tensor-core prefill reading the prefix itself)."""
+    prefix = 512
+    b = make_batch([prefix + 30, prefix + 200, prefix + 9], [1, 40, 9], 32, 8, seed=79,
+                   device="cuda", pool_factor=1.0, shared_prefix_tokens=prefix)
+    out, expected = _cascade_fp8(b, prefix // 16, 79)
+    compare(out, expected, what="fp8 cascade mixed")
+
+
 def test_attend_fp8_close_to_bf16_attention_of_the_same_rows(pkvlib):
     """Same batch, bf16 pool vs the FP8 pool written from the same rows: the
     two results agree to the accuracy of E4M3 (a sanity check of scale
@@ -248,13 +297,13 @@ def test_attend_fp8_rejects_bad_arguments(pkvlib):
     import ctypes
     P = pkv._ptr
     args = lambda ksp: (P(b.q), P(kc), P(vc), ksp, P(vs), P(meta["block_tables"]), P(meta["seq_lens"]),
-                        P(meta["query_start_loc"]), b.B, b.T, 0, ctypes.c_float(b.scale), P(out), P(ws),
+                        P(meta["query_start_loc"]), b.B, b.T, 0, 0, ctypes.c_float(b.scale), P(out), P(ws),
                         ws.numel(), ctypes.byref(desc), pkv._stream(b.q.device, None))
     assert lib.pkv_attend_fp8(*args(ctypes.c_void_p(0))) == -1          # PKV_ERR_NULL
     assert lib.pkv_attend_fp8(*args(ctypes.c_void_p(ks.data_ptr() + 1))) == -2  # PKV_ERR_ALIGN
     assert lib.pkv_attend_fp8(*args(P(ks))) == 0
     short = ctypes.c_size_t(ws.numel() - 256)
     a = list(args(P(ks)))
-    a[14] = short
+    a[15] = short
     assert lib.pkv_attend_fp8(*a) == -5  # PKV_ERR_WORKSPACE
     torch.cuda.synchronize()
