@@ -94,7 +94,7 @@ unsigned* status_word(int device) {
 static int make_ctx(pkv_stream_t stream, LaunchCtx* ctx) {
   int err = PKV_OK;
   const DeviceInfo* dev = current_device(&err);
-  if (!dev) return err;
+  if (!dev) return err != PKV_OK ? err : PKV_ERR_DEVICE;
   ctx->stream = reinterpret_cast<cudaStream_t>(stream);
   ctx->dev = dev;
   ctx->status = g_status_addr[dev->device];
@@ -156,7 +156,7 @@ int pkv_write(const pkv_bf16* k_new, const pkv_bf16* v_new, const int64_t* slot_
   if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
       !aligned(v_cache, 16) || !aligned(slot_mapping, 8))
     return PKV_ERR_ALIGN;
-  LaunchCtx ctx;
+  LaunchCtx ctx{};
   if (int e = make_ctx(stream, &ctx)) return e;
   return launch_write(ctx, k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache,
                       desc->num_blocks, desc->num_kv_heads);
@@ -202,7 +202,7 @@ int pkv_attend(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cac
       !aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(query_start_loc, 4) ||
       !aligned(workspace, 256))
     return PKV_ERR_ALIGN;
-  LaunchCtx ctx;
+  LaunchCtx ctx{};
   if (int e = make_ctx(stream, &ctx)) return e;
   AttendArgs a{q,          k_cache,    v_cache,    block_tables,  seq_lens,
                query_start_loc, num_seqs, num_tokens, max_query_len, shared_prefix_pages,
@@ -221,7 +221,7 @@ int pkv_write_fp8(const pkv_bf16* k_new, const pkv_bf16* v_new, const int64_t* s
   if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
       !aligned(v_cache, 16) || !aligned(slot_mapping, 8))
     return PKV_ERR_ALIGN;
-  LaunchCtx ctx;
+  LaunchCtx ctx{};
   if (int e = make_ctx(stream, &ctx)) return e;
   return launch_write_fp8(ctx, k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, k_scale,
                           v_scale, desc->num_blocks, desc->num_kv_heads);
@@ -244,7 +244,7 @@ int pkv_attend_fp8(const pkv_bf16* q, const pkv_fp8* k_cache, const pkv_fp8* v_c
       !aligned(v_scale, 16) || !aligned(out, 16) || !aligned(block_tables, 4) ||
       !aligned(seq_lens, 4) || !aligned(query_start_loc, 4) || !aligned(workspace, 256))
     return PKV_ERR_ALIGN;
-  LaunchCtx ctx;
+  LaunchCtx ctx{};
   if (int e = make_ctx(stream, &ctx)) return e;
   AttendArgs a{q,     k_cache, v_cache,   block_tables,    seq_lens, query_start_loc,
                num_seqs, num_tokens, max_query_len, shared_prefix_pages, scale, out, workspace,
@@ -257,7 +257,7 @@ int pkv_attend_fp8(const pkv_bf16* q, const pkv_fp8* k_cache, const pkv_fp8* v_c
 
 int pkv_get_last_error(pkv_stream_t stream, uint32_t* flags) {
   if (!flags) return PKV_ERR_NULL;
-  LaunchCtx ctx;
+  LaunchCtx ctx{};
   if (int e = make_ctx(stream, &ctx)) return e;
   unsigned host = 0;
   if (cudaMemcpyAsync(&host, ctx.status, sizeof(unsigned), cudaMemcpyDeviceToHost, ctx.stream) !=
