@@ -521,12 +521,16 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
       }
     }
   };
-  // The first pages of the ring into L2 while the previous kernel (normally
-  // pkv_write) is still running; the copies into shared memory wait below.
-  // (bf16 pages: 1 % on the 8B-shaped batch; the FP8 variant ran 2 % slower.)
+  // Each warp's first pages into L2 while the previous kernel (normally
+  // pkv_write, whose step leaves HBM idle) is still running; the copies into
+  // shared memory wait below.  bf16 pages: the ring's two pages and four more
+  // (1824 warps x 6 pages x 8 KiB = 88 MB, under the 129 MB L2): the
+  // 8B-shaped step 116 -> 112 us, the long-tail and mixed steps unchanged.
+  // Behind a shared-prefix pass (which reads the prefix from L2) only the
+  // ring's pages: six made that step 4 % slower; FP8 pages: none (2 % slower).
   if constexpr (!F8) {
     Cursor c = pc;
-    const int npf = min(NS, n_units);
+    const int npf = min(p.np > 0 ? NS : NS + 4, n_units);
     for (int s = 0; s < npf; ++s) {
       if (lane == 0) {
         constexpr int PB = kPageBytesOf<F8>;
