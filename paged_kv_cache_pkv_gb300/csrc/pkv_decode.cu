@@ -230,6 +230,24 @@ __device__ __forceinline__ void cursor_bid(Cursor& c, const DecodeParams& p) {
   c.bid = bid;
 }
 
+// The cursor one unit on, without reading the new unit's block id.
+__device__ __forceinline__ void cursor_step(Cursor& c, int np, const SeqSmem& sq, int per_row) {
+  if (++c.page == c.npages) {
+    c.page = 0;
+    c.item_start += c.npages;
+    if (++c.item == per_row) {
+      c.item = 0;
+      if (++c.j == c.n) {
+        c.j = 0;
+        int b = c.b + 1;
+        while (sq.start[b + 1] == sq.start[b]) ++b;
+        cursor_seq(c, sq, b);
+      }
+      cursor_row(c, np);
+    }
+  }
+}
+
 __device__ __forceinline__ void cursor_advance(Cursor& c, const DecodeParams& p,
                                                const SeqSmem& sq, int per_row) {
   if (++c.page == c.npages) {
@@ -528,18 +546,21 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
   // 8B-shaped step 116 -> 112 us, the long-tail and mixed steps unchanged.
   // Behind a shared-prefix pass (which reads the prefix from L2) only the
   // ring's pages: six made that step 4 % slower; FP8 pages: none (2 % slower).
+  // Lane s takes unit s: the block-id reads go out together.
   if constexpr (!F8) {
-    Cursor c = pc;
     const int npf = min(p.np > 0 ? NS : NS + 4, n_units);
-    for (int s = 0; s < npf; ++s) {
-      if (lane == 0) {
+    if (lane < npf) {
+      Cursor c = pc;
+      for (int s = 0; s < lane; ++s) cursor_step(c, p.np, sq, per_row);
+      int bid = __ldg(p.block_tables + int64_t(c.b) * p.max_blocks + p.np + c.page);
+      if (bid >= 0 && bid < p.num_blocks) {  // a bad id is flagged when its page is copied
         constexpr int PB = kPageBytesOf<F8>;
-        const size_t ph = size_t(c.bid) * p.Hkv + c.item / p.nsub;
+        const size_t ph = size_t(bid) * p.Hkv + c.item / p.nsub;
         prefetch_l2(p.k_cache + ph * PB, PB);
         prefetch_l2(p.v_cache + ph * PB, PB);
       }
-      if (s + 1 < npf) cursor_advance(c, p, sq, per_row);
     }
+    __syncwarp();
   }
   griddep_wait();
   {
