@@ -165,9 +165,10 @@ PKV_API int pkv_attend_workspace_size(const pkv_desc* desc, int32_t num_seqs,
  *                 256-byte aligned; contents need no initialisation.
  * Query head h reads kv head h / (num_q_heads/num_kv_heads).
  * Stream order: when pkv_attend directly follows pkv_write on a stream, its
- * set-up (reading seq_lens, query_start_loc and block_tables) overlaps the
- * write kernel through programmatic dependent launch; the pools are read only
- * after the write has finished.  Those three arrays must therefore not be
+ * set-up (reading seq_lens, query_start_loc and block_tables, and L2
+ * prefetch hints for the first pages) overlaps the write kernel through
+ * programmatic dependent launch; the pools are read only after the write has
+ * finished.  Those three arrays must therefore not be
  * written by the pkv_write call right before it (pkv_write never does). */
 PKV_API int pkv_attend(const pkv_bf16* q, const pkv_bf16* k_cache,
                const pkv_bf16* v_cache, const int32_t* block_tables,

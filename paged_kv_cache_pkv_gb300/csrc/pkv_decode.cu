@@ -428,9 +428,10 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
     fence_mbar_init();
   }
   // Under programmatic dependent launch everything up to griddep_wait() below
-  // (plan, cursor, first block ids) overlaps the previous kernel.  It reads
-  // only seq_lens, query_start_loc and block_tables, which pkv_write never
-  // writes; the pools are read only after the wait.
+  // (plan, cursor, first block ids, L2 prefetch hints) overlaps the previous
+  // kernel (pkv_write, or the chunked-prefill pass).  It reads only seq_lens,
+  // query_start_loc and block_tables, which neither writes; the pools and the
+  // workspace records are read only after the wait.
 
   // ---- plan: per-sequence unit counts and their exclusive prefix ----------
   const int per_row = p.Hkv * p.nsub;

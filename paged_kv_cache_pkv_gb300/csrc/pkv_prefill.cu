@@ -341,6 +341,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
+  // Let the split-KV kernel that follows start on the SMs this grid leaves
+  // free: its set-up and its L2 prefetch of the first pages overlap this
+  // compute-bound pass (it waits for this grid before reading what this
+  // writes).  Mixed step 329 -> 323 us.  Not for the shared-prefix pass: there
+  // it made the step 6 % slower.
+  if constexpr (!PREFIX) asm volatile("griddepcontrol.launch_dependents;");
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = sm + kOffQ;  // [tile u][2 halves]
   uint8_t* sK = sm + kOffK;
