@@ -1046,9 +1046,10 @@ int prefix_chunks(const pkv_desc& d, int32_t num_tokens, int32_t prefix_pages, i
   const int tg = tile_tokens(d);  // query tokens per CTA of the prefix pass (one Q tile)
   const int qgroups = (num_tokens + tg - 1) / tg;
   const int ntiles = (prefix_pages * kPage + kPfKeys - 1) / kPfKeys;
-  // split the prefix keys until the pass has about one CTA per SM (152), at
-  // most 16 chunks (the split-KV merge holds one chunk per lane of a half warp)
-  const int want = min(16, max(1, (152 + qgroups * d.num_kv_heads - 1) / (qgroups * d.num_kv_heads)));
+  // split the prefix keys into as many chunks as keep the pass to one wave
+  // (one CTA per SM, 152 SMs), at most 16 (the split-KV merge holds one chunk
+  // per lane of a half warp)
+  const int want = min(16, max(1, 152 / (qgroups * d.num_kv_heads)));
   const int per = max(1, (ntiles + want - 1) / want);
   *chunk_tiles = per;
   return (ntiles + per - 1) / per;
