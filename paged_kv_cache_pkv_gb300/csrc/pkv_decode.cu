@@ -79,6 +79,10 @@ struct DecodeParams {
   int32_t B, T, num_blocks, Hkv, Hq, G, nsub, max_blocks, simt_max_q, nwarps;
   float qscale;  // scale * log2(e)
   unsigned long long epoch;  // 48-bit call tag, never 0
+  // 0 when the kernel right before this one is this call's chunked-prefill
+  // pass, whose results this kernel never reads (its own inputs were
+  // complete before that pass started): then it runs beside the pass
+  int32_t wait_prev;
   // shared prefix: the first np pages of every row were attended by the
   // prefix pass, whose partial records (chunks per row and head) are merged
   int32_t np, chunks;
@@ -563,7 +567,7 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
     }
     __syncwarp();
   }
-  griddep_wait();
+  if (p.wait_prev) griddep_wait();
   {
     const int prologue = min(NS, n_units);
     for (int s = 0; s < prologue; ++s) {
@@ -1254,6 +1258,7 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   dp.nwarps = nwarps;
   dp.qscale = a.scale * 1.4426950408889634f;
   dp.epoch = next_epoch();
+  dp.wait_prev = (prefill && a.shared_prefix_pages == 0) ? 0 : 1;
   dp.np = a.shared_prefix_pages;
   dp.chunks = chunks;
   dp.prefix_part = reinterpret_cast<const float*>(ws + L.prefix);
