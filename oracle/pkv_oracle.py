@@ -24,7 +24,7 @@ What the pages fix, and what this oracle follows
   under a single-writer contract.
 
 The pages print no attention formula, no cache layout and no kernel.  The
-readings taken where they are silent (all listed in the design doc):
+readings taken where they are silent:
   * pool layout ``[num_blocks, num_kv_heads, page_size, head_dim]``;
   * ``seq_lens[b]`` counts the tokens written this step;
   * causal alignment is bottom-right: the n queries of sequence b are its last
@@ -244,7 +244,7 @@ def merge_partials(parts):
 # m * 2^-9; S.1111.111 is NaN; there are no infinities, so the largest finite
 # magnitude is 1.75 * 2^8 = 448.
 #
-# Readings taken here (listed in the design doc):
+# Readings taken here:
 #   * one scale per (page, kv head, row): a page fills one token per decode
 #     step, so a single per-page scale would force re-encoding rows already
 #     stored whenever a later token raised the page's maximum; a per-row scale
