@@ -169,7 +169,16 @@ PKV_API int pkv_attend_workspace_size(const pkv_desc* desc, int32_t num_seqs,
  * prefetch hints for the first pages) overlaps the write kernel through
  * programmatic dependent launch; the pools are read only after the write has
  * finished.  Those three arrays must therefore not be
- * written by the pkv_write call right before it (pkv_write never does). */
+ * written by the pkv_write call right before it (pkv_write never does).
+ * A call with query chunks longer than PKV_SPLITKV_MAX_QLEN runs its split-KV
+ * kernel and its tensor-core prefill kernel at the same time on disjoint
+ * SMs; work enqueued on the stream after the call still starts only once
+ * both have finished.  The SM share is sized by the environment variables
+ * PKV_PREFILL_STEP_UNITS (bf16 pages, default 1900) and
+ * PKV_PREFILL_STEP_UNITS_FP8 (default 6000), read once per process; 0 runs
+ * the prefill kernel first instead, with split-KV beside it on the SMs it
+ * leaves free.  With shared_prefix_pages > 0 the prefill kernel always runs
+ * first. */
 PKV_API int pkv_attend(const pkv_bf16* q, const pkv_bf16* k_cache,
                const pkv_bf16* v_cache, const int32_t* block_tables,
                const int32_t* seq_lens, const int32_t* query_start_loc,

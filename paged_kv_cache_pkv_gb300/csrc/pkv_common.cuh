@@ -55,6 +55,11 @@ constexpr uint64_t kDrainLimitNs = 2ull * 1000 * 1000;   // 2 ms for the clean-u
 // and l; padded to a 16-byte multiple.
 constexpr int kPrefixRec = 132;
 
+// Tensor-core prefill tiles: a Q tile is kPfRows query rows (kPfRows / G
+// tokens x the G heads of one kv head), a K/V tile kPfKeys keys (8 pages).
+constexpr int kPfRows = 128;
+constexpr int kPfKeys = 128;
+
 // Most sequences one pkv_attend call may carry (the per-sequence unit prefix
 // of the split-KV plan lives in shared memory).
 constexpr int kMaxSeqs = 2048;
@@ -126,6 +131,24 @@ __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// Atomic add with acquire-release semantics at GPU scope: publishes what the
+// caller wrote before it and, for the last arrival of a count, makes what the
+// other arrivals wrote visible.
+__device__ __forceinline__ unsigned long long atom_add_acq_rel(unsigned long long* p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their writes are visible (returns at once without one).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the grid launched after this one start once every CTA has executed
+// this or exited.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Wait for the phase with the given parity; false once limit_ns have passed.

@@ -81,8 +81,16 @@ struct DecodeParams {
   unsigned long long epoch;  // 48-bit call tag, never 0
   // 0 when the kernel right before this one is this call's chunked-prefill
   // pass, whose results this kernel never reads (its own inputs were
-  // complete before that pass started): then it runs beside the pass
+  // complete before that pass started): then it runs beside the pass, and
+  // waits for it only before it exits, so that the call ends with both
   int32_t wait_prev;
+  // 1 when this call's chunked-prefill pass is launched right after this
+  // kernel: the plan leaves the pass some of the SMs (its K/V tile steps
+  // times pf_cost against this kernel's units), and once the pool writes are
+  // complete every CTA lets the pass launch.  `join` is the pass's exit
+  // counter, stamped with the epoch here.
+  int32_t lead, pf_cost;
+  unsigned long long* join;
   // shared prefix: the first np pages of every row were attended by the
   // prefix pass, whose partial records (chunks per row and head) are merged
   int32_t np, chunks;
@@ -113,15 +121,6 @@ struct DecMeta {
   StageDesc desc[F8 ? kDecStagesF8 : kDecStages];
   uint64_t bar[F8 ? kDecStagesF8 : kDecStages];
 };
-
-// Atomic add with acquire-release semantics at GPU scope: publishes the
-// warp's partial (ordered before it by __syncwarp) and, for the last arrival,
-// makes every other warp's partial visible.
-__device__ __forceinline__ unsigned long long atom_add_acq_rel(unsigned long long* p, unsigned long long v) {
-  unsigned long long old;
-  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
-  return old;
-}
 
 // 2^(byte - 127) for a scale byte in [1, 254]; 0 for byte 0.
 __device__ __forceinline__ float scale_of(uint32_t byte) { return __uint_as_float(byte << 23); }
@@ -186,8 +185,6 @@ constexpr int kDecThreads = kDecWarps * 32;
 constexpr float kTau = 8.0f;  // log2-domain slack before the running max moves
 constexpr int kMinChunk = 4;  // fewest pages a decode warp is given
 constexpr unsigned kFull = 0xffffffffu;
-
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Sum over positions p in (0, x] of ceil(p / 16): pages of rows with those
 // visible-key counts.
@@ -445,6 +442,11 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
   // arrival that still sees an old epoch adds again once it is stamped.
   for (int i = blockIdx.x * NT + threadIdx.x; i < p.T * per_row; i += gridDim.x * NT)
     atomicExch(p.counters + i, p.epoch << 16);
+  // the prefill pass launched after this kernel counts its exits here (it
+  // launches only once this CTA has passed its trigger below, or exited)
+  if (p.lead && blockIdx.x == 0 && threadIdx.x == 0) atomicExch(p.join, p.epoch << 16);
+  __shared__ long long s_pfw[NW];
+  long long lead_steps = 0;  // lead: K/V tile steps of the prefill pass, all its CTAs
   {
     const int tid = threadIdx.x;
     const int per = (p.B + NT - 1) / NT;
@@ -470,6 +472,19 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
       }
       s_start[b] = units;
       local += units;
+      if (p.lead && !bad && n > p.simt_max_q) {
+        // the pass's CTAs: per kv head, groups of two Q tiles; a group's
+        // steps are the K/V tiles up to its last query's position
+        const int tg = 2 * (kPfRows / p.G);
+        long long st = 0;
+        for (int t0 = 0; t0 < n; t0 += tg) st += (L - n + min(n, t0 + tg) - 1) / kPfKeys + 1;
+        lead_steps += st * p.Hkv;
+      }
+    }
+    if (p.lead) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lead_steps += __shfl_xor_sync(kFull, lead_steps, o);
+      if (lane == 0) s_pfw[wib] = lead_steps;
     }
     int incl = local;
 #pragma unroll
@@ -493,13 +508,37 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
     }
     if (tid == 0) s_start[p.B] = total;
     __syncthreads();
+    if (p.lead) {
+      lead_steps = 0;
+#pragma unroll
+      for (int x = 0; x < NW; ++x) lead_steps += s_pfw[x];
+    }
   }
   const int U = s_start[p.B];
+  // Warps that take part.  With the prefill pass launched after this kernel,
+  // the last `psm` CTAs leave their SMs to it.  This kernel is bound by HBM,
+  // not by its SM count, so it takes about as long on fewer SMs; the pass is
+  // given enough SMs to finish its tile steps in that time, pf_cost being
+  // the units this kernel streams (whole GPU) while one SM does one step: at
+  // least one SM, at most half the grid.  Every CTA computes the same count.
+  int nw = p.nwarps;
+  if (p.lead && lead_steps > 0) {
+    const long long ncta = gridDim.x;
+    const long long want = U > 0 ? (lead_steps * p.pf_cost + U - 1) / U : ncta;
+    const int psm = int(min(ncta / 2, max(1ll, want)));
+    nw = (int(ncta) - psm) * NW;
+  }
   // equal contiguous ranges, at least kMinChunk pages so small batches do not
   // shatter into one-page partials
-  const int chunk = max(kMinChunk, (U + p.nwarps - 1) / p.nwarps);
+  const int chunk = max(kMinChunk, (U + nw - 1) / nw);
   const int w = blockIdx.x * NW + wib;
-  if (w >= p.nwarps || int64_t(w) * chunk >= U) return;
+  if (w >= nw || int64_t(w) * chunk >= U) {
+    // lead: this CTA's exit may let the prefill pass launch, which must not
+    // happen before the pool writes are complete; beside the pass: the call
+    // ends with this grid, so it must not end before the pass
+    if (p.lead || !p.wait_prev) griddep_wait();
+    return;
+  }
   const int u_begin = w * chunk;
   const int n_units = min(U - u_begin, chunk);
   const uint64_t policy = l2_evict_first_policy();
@@ -568,6 +607,7 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
     __syncwarp();
   }
   if (p.wait_prev) griddep_wait();
+  if (p.lead) griddep_launch_dependents();
   {
     const int prologue = min(NS, n_units);
     for (int s = 0; s < prologue; ++s) {
@@ -1098,9 +1138,11 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
     // let copies still in flight land before the CTA's shared memory is released
     for (int k = it; k < min(n_units, it + NS); ++k)
       mbar_wait(&M.bar[k % NS], (k / NS) & 1, kDrainLimitNs);
+    if (!p.wait_prev) griddep_wait();
     return;
   }
   if (cur_row >= 0) flush_segment();
+  if (!p.wait_prev) griddep_wait();  // beside the prefill pass: end after it
 }
 
 // ---------------------------------------------------------------------------
@@ -1140,6 +1182,25 @@ int decode_ctas_per_sm(int variant, bool fp8) {
     case 1: return fp8 ? occupancy_for<2, true>() : occupancy_for<2, false>();
     default: return fp8 ? occupancy_for<4, true>() : occupancy_for<4, false>();
   }
+}
+
+// Split-KV units (one page of one kv head, K and V) the whole GPU streams
+// while one SM runs one K/V tile step of the prefill pass: bf16 pages about
+// 2.4 us per step (two Q tiles) against 6.5 TB/s / 8 KiB per unit.  Sizes the
+// SM share the split-KV kernel leaves the pass when the pass runs behind it;
+// 0 puts the pass first instead.  Measured on the 96-row mixed step (two
+// 512-token chunks): bf16 1200 / 1900 / 2800 -> 278 / 269 / 272 us (pass
+// first: 306 us).  FP8 pages (the pass widens codes, about 5.6 us a step):
+// 3000 / 6000 -> 342 / 319 us (pass first: 340 us); 6000 already gives the
+// pass its cap of half the SMs there.
+static int prefill_step_units(bool fp8) {
+  static int v[2] = {-1, -1};
+  int& x = v[fp8 ? 1 : 0];
+  if (x < 0) {
+    const char* e = getenv(fp8 ? "PKV_PREFILL_STEP_UNITS_FP8" : "PKV_PREFILL_STEP_UNITS");
+    x = e ? atoi(e) : (fp8 ? 6000 : 1900);
+  }
+  return x;
 }
 
 // Sequences with more query rows than this go to the tensor-core prefill
@@ -1225,8 +1286,16 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   const bool prefill = max_tiles > 0 && a.num_tokens > simt_max_q() &&
                        (a.max_query_len <= 0 || a.max_query_len > simt_max_q());
   const int split_max_q = prefill ? simt_max_q() : INT_MAX;
-  if (prefill) {
-    if (int e = launch_prefill(ctx, a, ws + L.tiles, split_max_q, max_tiles)) return e;
+  // Without a shared prefix: split-KV first, on the SMs its plan keeps, and
+  // the prefill pass behind it on the rest.  Otherwise the pass first and
+  // split-KV beside it on the SMs it leaves free.
+  const int pf_cost = prefill_step_units(a.fp8);
+  const bool lead = prefill && a.shared_prefix_pages == 0 && pf_cost > 0 &&
+                    int64_t(d.num_kv_heads) * prefill_groups(d, a.num_seqs, a.num_tokens, max_tiles) < 0xFFFF;
+  const unsigned long long epoch = next_epoch();
+  unsigned long long* join = reinterpret_cast<unsigned long long*>(ws + L.tiles);
+  if (prefill && !lead) {
+    if (int e = launch_prefill(ctx, a, split_max_q, max_tiles, nullptr, 0)) return e;
   }
   if (a.shared_prefix_pages > 0) {
     if (int e = launch_prefix(ctx, a, reinterpret_cast<float*>(ws + L.prefix), chunks, chunk_tiles))
@@ -1257,8 +1326,11 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   dp.simt_max_q = split_max_q;
   dp.nwarps = nwarps;
   dp.qscale = a.scale * 1.4426950408889634f;
-  dp.epoch = next_epoch();
-  dp.wait_prev = (prefill && a.shared_prefix_pages == 0) ? 0 : 1;
+  dp.epoch = epoch;
+  dp.wait_prev = (prefill && !lead && a.shared_prefix_pages == 0) ? 0 : 1;
+  dp.lead = lead ? 1 : 0;
+  dp.pf_cost = pf_cost;
+  dp.join = lead ? join : nullptr;
   dp.np = a.shared_prefix_pages;
   dp.chunks = chunks;
   dp.prefix_part = reinterpret_cast<const float*>(ws + L.prefix);
@@ -1278,18 +1350,22 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
         !encode_tensor_map(&tv, dt, a.v_cache, 2, dims, strides, box))
       return PKV_ERR_LAUNCH;
   }
+  int e;
   if (a.fp8) {
     switch (GH) {
-      case 1: return launch_decode<1, true>(ctx, dp, tk, tv);
-      case 2: return launch_decode<2, true>(ctx, dp, tk, tv);
-      default: return launch_decode<4, true>(ctx, dp, tk, tv);
+      case 1: e = launch_decode<1, true>(ctx, dp, tk, tv); break;
+      case 2: e = launch_decode<2, true>(ctx, dp, tk, tv); break;
+      default: e = launch_decode<4, true>(ctx, dp, tk, tv); break;
+    }
+  } else {
+    switch (GH) {
+      case 1: e = launch_decode<1, false>(ctx, dp, tk, tv); break;
+      case 2: e = launch_decode<2, false>(ctx, dp, tk, tv); break;
+      default: e = launch_decode<4, false>(ctx, dp, tk, tv); break;
     }
   }
-  switch (GH) {
-    case 1: return launch_decode<1, false>(ctx, dp, tk, tv);
-    case 2: return launch_decode<2, false>(ctx, dp, tk, tv);
-    default: return launch_decode<4, false>(ctx, dp, tk, tv);
-  }
+  if (e || !lead) return e;
+  return launch_prefill(ctx, a, split_max_q, max_tiles, join, epoch);
 }
 
 }  // namespace pkv

@@ -84,10 +84,14 @@ int decode_ctas_per_sm(int variant, bool fp8);
 
 // Tensor-core chunked-prefill path (pkv_prefill.cu).
 int prefill_max_tiles(const pkv_desc& d, int32_t num_seqs, int32_t num_tokens);
+// CTAs per kv head of the prefill launch.
+int prefill_groups(const pkv_desc& d, int32_t num_seqs, int32_t num_tokens, int max_tiles);
 // Launches the prefill kernel for sequences with more than split_max_q query
-// rows; `scratch` is the workspace's tile area.
-int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, void* scratch, int split_max_q,
-                   int max_tiles);
+// rows.  join == null: it runs first (normal launch).  Otherwise it is
+// launched behind this call's split-KV kernel, which stamped `join` (an
+// 8-byte workspace word) with `epoch`.
+int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, int split_max_q, int max_tiles,
+                   unsigned long long* join, unsigned long long epoch);
 // Shared-prefix pass: key chunks of the prefix and tiles per chunk.
 // A tiled TMA descriptor with 128-byte swizzle (rank <= 3; strides in bytes
 // for dims 1..rank-1).  Returns false when the driver entry point is missing

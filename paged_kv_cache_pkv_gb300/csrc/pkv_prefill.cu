@@ -61,7 +61,6 @@ namespace pkv {
 
 constexpr int kPfSoftmaxThreads = 256;  // two threads per query row (64 score columns each)
 constexpr int kPfThreads = kPfSoftmaxThreads + 128;  // + K-load, V-load and two MMA warps
-constexpr int kPfKeys = 128;          // keys per K/V tile (8 pages)
 constexpr int kPfPagesPerTile = kPfKeys / kPage;
 constexpr uint32_t kTmemCols = 512;   // S/P of Q tile 0 [0,128), of tile 1 [128,256), O0 [256,384), O1 [384,512)
 constexpr float kPfTau = 8.0f;
@@ -107,7 +106,30 @@ struct PrefillParams {
   // FP8 pages: row scale bytes [NB][Hkv][16] of K and V (null for bf16 pages)
   const uint8_t* k_scale;
   const uint8_t* v_scale;
+  // Launched after the split-KV kernel of the same call, which runs on: every
+  // CTA counts its exit here (the split-KV kernel stamped the word with this
+  // epoch) and the last one waits for that kernel, so the call ends with
+  // both.  Null when this pass runs first.
+  unsigned long long* join;
+  unsigned long long epoch;
 };
+
+// Exit of a CTA (thread 0): count it; the last of the grid waits for the
+// split-KV kernel this pass was launched behind.
+__device__ __forceinline__ void join_exit(const PrefillParams& p) {
+  if (!p.join) return;
+  const unsigned long long total = static_cast<unsigned long long>(gridDim.x) * gridDim.y;
+  unsigned long long v = atom_add_acq_rel(p.join, 1ull);
+  const uint64_t t0 = global_ns();
+  while ((v >> 16) != p.epoch) {  // not stamped yet: the stamp overwrites this add
+    if (global_ns() - t0 > kWaitLimitNs) {
+      flag_status(p.status, PKV_STATUS_TIMEOUT);
+      return;
+    }
+    v = atom_add_acq_rel(p.join, 1ull);
+  }
+  if ((v & 0xFFFFull) + 1 == total) griddep_wait();
+}
 
 // ---------------------------------------------------------------------------
 // tcgen05 / TMA helpers
@@ -341,12 +363,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
-  // Let the split-KV kernel that follows start on the SMs this grid leaves
-  // free: its set-up and its L2 prefetch of the first pages overlap this
-  // compute-bound pass (it waits for this grid before reading what this
-  // writes).  Mixed step 329 -> 323 us.  Not for the shared-prefix pass: there
-  // it made the step 6 % slower.
-  if constexpr (!PREFIX) asm volatile("griddepcontrol.launch_dependents;");
+  // Run first (join == null): let the split-KV kernel that follows start on
+  // the SMs this grid leaves free, beside this compute-bound pass (it reads
+  // nothing this writes, and waits for this grid before it exits).  Mixed
+  // step 329 -> 306 us.  Not for the shared-prefix pass: there it made the
+  // step 6 % slower.  Run behind split-KV: no early start for what follows
+  // (the next call's split-KV kernel would stamp its counters while this
+  // call's still merges); it launches once every CTA here has exited, the
+  // last of them after the split-KV kernel completed.
+  if constexpr (!PREFIX) {
+    if (!p.join) griddep_launch_dependents();
+  }
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = sm + kOffQ;  // [tile u][2 halves]
   uint8_t* sK = sm + kOffK;
@@ -447,7 +474,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     __syncthreads();
     b = s_info[0];
-    if (b < 0) return;  // no work for this CTA (before any TMEM is taken)
+    if (b < 0) {  // no work for this CTA (before any TMEM is taken)
+      if (tid == 0) join_exit(p);
+      return;
+    }
     t0 = s_info[1];
     const int q0 = __ldg(p.qsl + b);
     n = __ldg(p.qsl + b + 1) - q0;
@@ -902,6 +932,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
   }
+  if (tid == 0) join_exit(p);
 }
 
 // ---------------------------------------------------------------------------
@@ -1017,24 +1048,39 @@ static PrefillParams make_params(const LaunchCtx& ctx, const AttendArgs& a, int 
   return pp;
 }
 
-int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, void* /*scratch*/, int split_max_q,
-                   int max_tiles) {
+int prefill_groups(const pkv_desc& d, int32_t num_seqs, int32_t num_tokens, int max_tiles) {
+  // one CTA per group of two Q tiles; every sequence may end in a partial group
+  const int tg = 2 * tile_tokens(d);
+  return min(max_tiles, (num_tokens + tg - 1) / tg + num_seqs);
+}
+
+int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, int split_max_q, int max_tiles,
+                   unsigned long long* join, unsigned long long epoch) {
   if (int e = a.fp8 ? ensure_prefill_attr<false, true>(ctx.dev->device)
                     : ensure_prefill_attr<false, false>(ctx.dev->device))
     return e;
   CUtensorMap tq, tk, tv;
   if (int e = make_maps(a, &tq, &tk, &tv)) return e;
-  const PrefillParams pp = make_params(ctx, a, split_max_q);
-  // one CTA per group of two Q tiles; every sequence may end in a partial group
-  const int tg = 2 * pp.TM;
-  const int groups = min(max_tiles, (a.num_tokens + tg - 1) / tg + a.num_seqs);
+  PrefillParams pp = make_params(ctx, a, split_max_q);
+  pp.join = join;
+  pp.epoch = epoch;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.desc.num_kv_heads, prefill_groups(a.desc, a.num_seqs, a.num_tokens, max_tiles));
+  cfg.blockDim = dim3(kPfThreads);
+  cfg.dynamicSmemBytes = a.fp8 ? kPfSmemOf<true> : kPfSmemOf<false>;
+  cfg.stream = ctx.stream;
+  // behind the split-KV kernel: start once its CTAs let it (their pool reads
+  // begin after pkv_write completed, and so do this pass's)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = join ? 1 : 0;
   TraceScope ts(ctx.stream, PKV_K_PREFILL);
   if (a.fp8)
-    pkv_prefill_kernel<false, true><<<dim3(a.desc.num_kv_heads, groups), kPfThreads, kPfSmemOf<true>,
-                                      ctx.stream>>>(tq, tk, tv, pp);
+    cudaLaunchKernelEx(&cfg, pkv_prefill_kernel<false, true>, tq, tk, tv, pp);
   else
-    pkv_prefill_kernel<false, false><<<dim3(a.desc.num_kv_heads, groups), kPfThreads, kPfSmemOf<false>,
-                                       ctx.stream>>>(tq, tk, tv, pp);
+    cudaLaunchKernelEx(&cfg, pkv_prefill_kernel<false, false>, tq, tk, tv, pp);
   return ts.done();
 }
 

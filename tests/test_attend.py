@@ -180,6 +180,24 @@ def test_repeated_calls_reuse_workspace(pkvlib):
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
 
 
+def test_repeated_mixed_calls_reuse_workspace(pkvlib):
+    """Back-to-back calls with a prefill chunk and long split-KV work on one
+    workspace: a call's kernels must not overlap the previous call's merges."""
+    b = make_batch([3000] * 40 + [300], [1] * 40 + [200], 32, 8, seed=91, device="cuda")
+    meta = to_device(b)
+    kc, vc = b.k_cache.clone(), b.v_cache.clone()
+    pkv.write(b.k_new, b.v_new, meta["slot_mapping"], kc, vc)
+    ws = torch.empty(pkv.workspace_size(pkv.make_desc(kc, b.num_q_heads, b.block_tables.shape[1]),
+                                        b.B, b.T), dtype=torch.uint8, device="cuda")
+    outs = [pkv.attend(b.q, kc, vc, meta["block_tables"], meta["seq_lens"], meta["query_start_loc"],
+                       b.scale, workspace=ws) for _ in range(4)]
+    torch.cuda.synchronize()
+    assert pkv.get_last_error() == 0
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
+    k_ref, v_ref = oracle_write(b)
+    compare(outs[-1], oracle_attend(b, k_ref, v_ref), what="repeated mixed calls")
+
+
 def _kernel_launches(batch, max_query_len):
     meta = to_device(batch)
     kc, vc = batch.k_cache.clone(), batch.v_cache.clone()
@@ -225,6 +243,29 @@ def test_prefill_chunks_of_several_sequences(pkvlib):
     assert counts["prefill"] == 1
     k_ref, v_ref = oracle_write(b)
     compare(out, oracle_attend(b, k_ref, v_ref), what="several prefill chunks")
+
+
+@pytest.mark.parametrize("lens,qlens", [
+    ([3000] * 40 + [300], [1] * 40 + [200]),  # long split-KV work, short prefill chunk
+    ([2048, 64], [512, 1]),                   # long prefill chunk, short split-KV work
+    ([700, 500], [300, 200]),                 # prefill chunks only
+])
+def test_mixed_step_result_is_stream_ordered(pkvlib, lens, qlens):
+    """A copy ordered on the stream right after pkv_attend (no device-wide
+    synchronisation) reads the complete output, whichever of the split-KV
+    kernel and the prefill pass finishes last."""
+    b = make_batch(lens, qlens, 32, 8, seed=sum(lens), device="cuda")
+    meta = to_device(b)
+    kc, vc = b.k_cache.clone(), b.v_cache.clone()
+    out = torch.full_like(b.q, float("nan"))
+    torch.cuda.synchronize()
+    pkv.write(b.k_new, b.v_new, meta["slot_mapping"], kc, vc)
+    pkv.attend(b.q, kc, vc, meta["block_tables"], meta["seq_lens"], meta["query_start_loc"], b.scale,
+               out=out)
+    host = out.cpu()  # stream-ordered copy
+    assert pkv.get_last_error() == 0
+    k_ref, v_ref = oracle_write(b)
+    compare(host, oracle_attend(b, k_ref, v_ref), what=f"stream-ordered read {len(lens)} rows")
 
 
 def _cascade(batch, prefix_pages, max_query_len=0):

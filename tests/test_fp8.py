@@ -184,6 +184,29 @@ def test_attend_fp8_prefill_chunks_all_rows(pkvlib, hq, hkv, L, n):
     assert counts["prefill"] == 1
 
 
+@pytest.mark.parametrize("lens,qlens", [
+    ([2048, 64], [512, 1]),                   # long prefill chunk, short split-KV work
+    ([3000] * 40 + [300], [1] * 40 + [200]),  # long split-KV work, short prefill chunk
+])
+def test_attend_fp8_mixed_step_result_is_stream_ordered(pkvlib, lens, qlens):
+    """A copy ordered on the stream right after pkv_attend_fp8 (no device-wide
+    synchronisation) reads the complete output, whichever kernel ends last."""
+    b = make_batch(lens, qlens, 32, 8, seed=sum(lens) + 1, device="cuda")
+    pools = fp8_pools(b, 41)
+    meta = to_device(b)
+    g = _gpu_write(b, pools, meta)
+    out = torch.full_like(b.q, float("nan"))
+    torch.cuda.synchronize()
+    pkv.attend_fp8(b.q, *g, meta["block_tables"], meta["seq_lens"], meta["query_start_loc"], b.scale,
+                   out=out)
+    host = out.cpu()  # stream-ordered copy
+    assert pkv.get_last_error() == 0
+    ref = _oracle_write(b, pools)
+    expected = O.attend_fp8(bits(b.q), *ref, b.block_tables, b.seq_lens, b.query_start_loc, b.scale,
+                            b.num_q_heads, b.num_kv_heads, b.page_size)
+    compare(host, expected, what=f"fp8 stream-ordered read {len(lens)} rows")
+
+
 def test_attend_fp8_prefill_stale_rows_do_not_leak(pkvlib):
     """A prefill chunk whose last page is partly past the sequence: those rows
     hold NaN codes and scale bytes 0 and 255, and must not reach the output."""
