@@ -80,11 +80,38 @@ def job_throughput(units_local, seconds_local, world, device=None):
     return units_local / seconds_local, seconds_local, units_local
 
 
-def kernel_hash():
+def code_tokens(text):
+    """C++ source with comments removed and whitespace collapsed: what the
+    compiler sees, so that editing a comment keeps a profile valid."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # string or character literal, kept whole
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def kernel_hash(root=ROOT):
+    """Hash of the decode kernel's code (comments excluded), recorded beside
+    the ncu counters in the profile summary."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(root, f), encoding="utf-8") as fh:
+            h.update(code_tokens(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -32,11 +32,11 @@
 //    operands come from registers, so the warp-level MMA is the fit.  It needs
 //    about a quarter of the instructions of packed FMAs, which lets a CTA run
 //    12 warps (168 registers) and hide more latency.
-//  * bf16 pages: bf16 operands as stored (q too), P rounded to bf16; pages by
-//    cp.async.bulk.  FP8 pages (template flag F8): 2 KiB pages of E4M3 codes
-//    by TMA tensor copies with 128-byte swizzle (conflict-free fragment reads)
-//    plus 16-byte blocks of per-row scale bytes (scale = 2^(byte-127)) by bulk
-//    copies; codes are widened exactly to f16 (E4M3 is a subset of f16), q is
+//  * bf16 pages: bf16 operands as stored (q too), P rounded to bf16; a page
+//    is one TMA tensor copy (the pool viewed as rows of 128 bytes, 128-byte
+//    swizzle: conflict-free fragment reads).  FP8 pages (template flag F8):
+//    2 KiB pages of E4M3 codes by the same kind of copy, plus 16-byte blocks
+//    of per-row scale bytes (scale = 2^(byte-127)) by bulk copies; codes are widened exactly to f16 (E4M3 is a subset of f16), q is
 //    scaled by a power of two into f16 range (exact), P is f16.  Row scales:
 //    the K one multiplies the finished score; the V one weights the
 //    probability relative to the largest V scale of the segment (a running
@@ -50,6 +50,10 @@
 //    an epoch-tagged arrival counter; the last warp to arrive merges the
 //    partials (log-sum-exp) and writes the output.  The epoch is new on every
 //    call, so the workspace never needs clearing.
+//  * Beside the tensor-core prefill pass of the same call: this kernel is
+//    launched first and its plan leaves the pass part of the SMs (sized from
+//    the pass's tile steps against this kernel's units); the pass, launched
+//    behind it, runs on those SMs at the same time.
 #include <atomic>
 #include <chrono>
 #include <climits>
@@ -433,9 +437,10 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
   }
   // Under programmatic dependent launch everything up to griddep_wait() below
   // (plan, cursor, first block ids, L2 prefetch hints) overlaps the previous
-  // kernel (pkv_write, or the chunked-prefill pass).  It reads only seq_lens,
-  // query_start_loc and block_tables, which neither writes; the pools and the
-  // workspace records are read only after the wait.
+  // kernel (pkv_write, the shared-prefix pass, or a chunked-prefill pass that
+  // runs first).  It reads only seq_lens, query_start_loc and block_tables,
+  // which none of them writes; the pools and the workspace records are read
+  // only after the wait.
 
   // ---- plan: per-sequence unit counts and their exclusive prefix ----------
   const int per_row = p.Hkv * p.nsub;
