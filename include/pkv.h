@@ -173,11 +173,11 @@ PKV_API int pkv_attend_workspace_size(const pkv_desc* desc, int32_t num_seqs,
  * A call with query chunks longer than PKV_SPLITKV_MAX_QLEN runs its split-KV
  * kernel and its tensor-core prefill kernel at the same time on disjoint
  * SMs; work enqueued on the stream after the call still starts only once
- * both have finished.  The SM share is sized by the environment variables
- * PKV_PREFILL_STEP_UNITS (bf16 pages, default 1900) and
- * PKV_PREFILL_STEP_UNITS_FP8 (default 6000), read once per process; 0 runs
- * the prefill kernel first instead, with split-KV beside it on the SMs it
- * leaves free.  With shared_prefix_pages > 0 the prefill kernel always runs
+ * both have finished.  The SM share follows the two kernels' work; it is
+ * scaled by the environment variables PKV_PREFILL_STEP_UNITS (bf16 pages,
+ * default 1900) and PKV_PREFILL_STEP_UNITS_FP8 (default 10000), read once
+ * per process; 0 runs the prefill kernel first instead, with split-KV beside
+ * it on the SMs it leaves free.  With shared_prefix_pages > 0 the prefill kernel always runs
  * first. */
 PKV_API int pkv_attend(const pkv_bf16* q, const pkv_bf16* k_cache,
                const pkv_bf16* v_cache, const int32_t* block_tables,

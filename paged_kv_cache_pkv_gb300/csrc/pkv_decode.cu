@@ -93,7 +93,9 @@ struct DecodeParams {
   // times pf_cost against this kernel's units), and once the pool writes are
   // complete every CTA lets the pass launch.  `join` is the pass's exit
   // counter, stamped with the epoch here.
-  int32_t lead, pf_cost;
+  // lead_sat: SMs at which this kernel's page stream saturates HBM (0: it
+  // never does, i.e. it is bound by the SMs it runs on)
+  int32_t lead, pf_cost, lead_sat;
   unsigned long long* join;
   // shared prefix: the first np pages of every row were attended by the
   // prefix pass, whose partial records (chunks per row and head) are merged
@@ -524,16 +526,26 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
   }
   const int U = s_start[p.B];
   // Warps that take part.  With the prefill pass launched after this kernel,
-  // the last `psm` CTAs leave their SMs to it.  This kernel is bound by HBM,
-  // not by its SM count, so it takes about as long on fewer SMs; the pass is
-  // given enough SMs to finish its tile steps in that time, pf_cost being
-  // the units this kernel streams (whole GPU) while one SM does one step: at
-  // least one SM, at most half the grid.  Every CTA computes the same count.
+  // the last `psm` CTAs leave their SMs to it; every CTA computes the same
+  // count.  The pass's work in this kernel's units is its tile steps times
+  // pf_cost (the units this kernel streams, whole GPU, while one SM does one
+  // step).  While at least lead_sat SMs stay here this kernel is bound by HBM
+  // and takes about as long as on all of them: the pass gets the SMs that
+  // finish its work in that time.  A larger pass leaves fewer SMs than that,
+  // and then both kernels' times scale with their SM counts: the SMs are
+  // split in proportion to the work (pass work : units x lead_sat / grid).
+  // At least one SM goes to the pass and one stays here.
   int nw = p.nwarps;
   if (p.lead && lead_steps > 0) {
     const long long ncta = gridDim.x;
-    const long long want = U > 0 ? (lead_steps * p.pf_cost + U - 1) / U : ncta;
-    const int psm = int(min(ncta / 2, max(1ll, want)));
+    const long long sat = p.lead_sat > 0 ? min(ncta, (long long)p.lead_sat) : ncta;
+    const long long work = lead_steps * p.pf_cost;
+    long long want = ncta - 1;
+    if (U > 0) {
+      want = (work + U - 1) / U;
+      if (want > ncta - sat) want = (work * ncta + work + U * sat - 1) / (work + U * sat);
+    }
+    const int psm = int(min(ncta - 1, max(1ll, want)));
     nw = (int(ncta) - psm) * NW;
   }
   // equal contiguous ranges, at least kMinChunk pages so small batches do not
@@ -1197,19 +1209,25 @@ int decode_ctas_per_sm(int variant, bool fp8) {
 // 2.4 us per step (two Q tiles) against 6.5 TB/s / 8 KiB per unit.  Sizes the
 // SM share the split-KV kernel leaves the pass when the pass runs behind it;
 // 0 puts the pass first instead.  Measured on the 96-row mixed step (two
-// 512-token chunks): bf16 1200 / 1900 / 2800 -> 278 / 269 / 272 us (pass
-// first: 306 us).  FP8 pages (the pass widens codes, about 5.6 us a step):
-// 3000 / 6000 -> 342 / 319 us (pass first: 340 us); 6000 already gives the
-// pass its cap of half the SMs there.
+// 512-token chunks; 2,880 steps against 188,544 units): bf16 1200 / 1900 /
+// 2800 -> 19 / 30 / 43 SMs for the pass -> 278 / 269 / 272 us (pass first:
+// 306 us).  FP8 pages (the pass widens codes, about 5.6 us a step, and
+// split-KV is bound by issue, so the SMs are split in proportion): 46 / 76
+// SMs for the pass -> 342 / 319 us (pass first: 340 us); 10000 gives 77.
 static int prefill_step_units(bool fp8) {
   static int v[2] = {-1, -1};
   int& x = v[fp8 ? 1 : 0];
   if (x < 0) {
     const char* e = getenv(fp8 ? "PKV_PREFILL_STEP_UNITS_FP8" : "PKV_PREFILL_STEP_UNITS");
-    x = e ? atoi(e) : (fp8 ? 6000 : 1900);
+    x = e ? atoi(e) : (fp8 ? 10000 : 1900);
   }
   return x;
 }
+
+// SMs at which the split-KV kernel's page stream saturates HBM.  bf16 pages:
+// on the mixed step it took 262-268 us on 122 SMs against 254 us on 152,
+// which puts saturation near 126.  FP8 pages: never (bound by issue).
+static int split_kv_saturating_sms(bool fp8) { return fp8 ? 0 : 126; }
 
 // Sequences with more query rows than this go to the tensor-core prefill
 // kernel (when it is built in); the rest go through split-KV.
@@ -1338,6 +1356,7 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   dp.wait_prev = (prefill && !lead && a.shared_prefix_pages == 0) ? 0 : 1;
   dp.lead = lead ? 1 : 0;
   dp.pf_cost = pf_cost;
+  dp.lead_sat = split_kv_saturating_sms(a.fp8);
   dp.join = lead ? join : nullptr;
   dp.np = a.shared_prefix_pages;
   dp.chunks = chunks;
