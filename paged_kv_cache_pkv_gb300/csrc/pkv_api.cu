@@ -144,6 +144,8 @@ int TraceScope::done() {
 
 using namespace pkv;
 
+static_assert(kMaxSeqs == PKV_MAX_SEQS, "the plan's shared-memory arrays hold PKV_MAX_SEQS sequences");
+
 extern "C" {
 
 int pkv_write(const pkv_bf16* k_new, const pkv_bf16* v_new, const int64_t* slot_mapping,
@@ -166,7 +168,9 @@ int pkv_attend_workspace_size(const pkv_desc* desc, int32_t num_seqs, int32_t nu
                               int32_t shared_prefix_pages, size_t* bytes) {
   if (int e = check_desc(desc)) return e;
   if (!bytes) return PKV_ERR_NULL;
-  if (num_seqs < 0 || num_tokens < 0 || shared_prefix_pages < 0) return PKV_ERR_RANGE;
+  if (num_seqs < 0 || num_seqs > PKV_MAX_SEQS || num_tokens < 0 || shared_prefix_pages < 0 ||
+      shared_prefix_pages > desc->max_blocks_per_seq)
+    return PKV_ERR_RANGE;
   int err = PKV_OK;
   const DeviceInfo* dev = current_device(&err);
   if (!dev) return err;
@@ -178,7 +182,9 @@ int pkv_attend_fp8_workspace_size(const pkv_desc* desc, int32_t num_seqs, int32_
                                   int32_t shared_prefix_pages, size_t* bytes) {
   if (int e = check_desc(desc)) return e;
   if (!bytes) return PKV_ERR_NULL;
-  if (num_seqs < 0 || num_tokens < 0 || shared_prefix_pages < 0) return PKV_ERR_RANGE;
+  if (num_seqs < 0 || num_seqs > PKV_MAX_SEQS || num_tokens < 0 || shared_prefix_pages < 0 ||
+      shared_prefix_pages > desc->max_blocks_per_seq)
+    return PKV_ERR_RANGE;
   int err = PKV_OK;
   const DeviceInfo* dev = current_device(&err);
   if (!dev) return err;
@@ -193,7 +199,9 @@ int pkv_attend(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cac
                void* workspace, size_t workspace_bytes, const pkv_desc* desc,
                pkv_stream_t stream) {
   if (int e = check_desc(desc)) return e;
-  if (num_seqs < 0 || num_tokens < 0) return PKV_ERR_RANGE;
+  if (num_seqs < 0 || num_seqs > PKV_MAX_SEQS || num_tokens < 0 || shared_prefix_pages < 0 ||
+      shared_prefix_pages > desc->max_blocks_per_seq)
+    return PKV_ERR_RANGE;
   if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start_loc || !out ||
       !workspace)
@@ -235,7 +243,9 @@ int pkv_attend_fp8(const pkv_bf16* q, const pkv_fp8* k_cache, const pkv_fp8* v_c
                    void* workspace, size_t workspace_bytes, const pkv_desc* desc,
                    pkv_stream_t stream) {
   if (int e = check_desc(desc)) return e;
-  if (num_seqs < 0 || num_tokens < 0) return PKV_ERR_RANGE;
+  if (num_seqs < 0 || num_seqs > PKV_MAX_SEQS || num_tokens < 0 || shared_prefix_pages < 0 ||
+      shared_prefix_pages > desc->max_blocks_per_seq)
+    return PKV_ERR_RANGE;
   if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !k_scale || !v_scale || !block_tables || !seq_lens ||
       !query_start_loc || !out || !workspace)

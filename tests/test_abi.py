@@ -84,6 +84,24 @@ def test_null_and_misaligned_pointers_rejected(pkvlib):
                              None, None) == -1
 
 
+def test_counts_out_of_range_rejected_before_any_device_work(pkvlib):
+    """More sequences than PKV_MAX_SEQS, or a shared prefix longer than a
+    block-table row, is a range error from every attention entry point and
+    from the workspace queries, checked before a device is touched."""
+    d = _desc()
+    before = pkvlib.pkv_launch_count()
+    assert _attend(pkvlib, d, B=2049, T=2049) == -4
+    assert pkvlib.pkv_attend(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4, 0, d.max_blocks_per_seq + 1, 0.1,
+                             FAKE, FAKE, 1 << 20, ctypes.byref(d), None) == -4
+    for prefix, B in ((0, 2049), (d.max_blocks_per_seq + 1, 4)):
+        assert pkvlib.pkv_attend_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, B, 0, prefix, 0.1,
+                                     FAKE, FAKE, 1 << 20, ctypes.byref(d), None) == -4
+        n = ctypes.c_size_t(0)
+        assert pkvlib.pkv_attend_workspace_size(ctypes.byref(d), B, B, prefix, ctypes.byref(n)) == -4
+        assert pkvlib.pkv_attend_fp8_workspace_size(ctypes.byref(d), B, B, prefix, ctypes.byref(n)) == -4
+    assert pkvlib.pkv_launch_count() == before
+
+
 def test_empty_calls_launch_nothing(pkvlib):
     d = _desc()
     before = pkvlib.pkv_launch_count()

@@ -167,6 +167,25 @@ def test_query_longer_than_sequence_is_flagged(pkvlib):
     assert pkv.get_last_error() & pkv.STATUS_BAD_QUERY
 
 
+def test_most_sequences_per_call(pkvlib):
+    """PKV_MAX_SEQS decode sequences in one call fill the plan's per-sequence
+    arrays in shared memory: every row against the oracle; one more sequence
+    is a range error.  32-64 keys per row: with only a few keys an output is
+    close to one V row (|out| near 4 on this data), where the bf16 output
+    rounding alone uses 7.8e-3 of the 1e-2 budget."""
+    lens = np.random.default_rng(2048).integers(32, 65, size=2048).tolist()
+    b = make_batch(lens, [1] * 2048, 8, 2, seed=2048, device="cuda")
+    check_batch(b, what="2048 sequences")
+    meta = to_device(b)
+    bt = torch.cat([meta["block_tables"], meta["block_tables"][:1]])
+    sl = torch.cat([meta["seq_lens"], meta["seq_lens"][:1]])
+    qsl = torch.arange(2050, dtype=torch.int32, device="cuda")
+    q = torch.cat([b.q, b.q[:1]])
+    with pytest.raises(pkv.PkvError) as err:
+        pkv.attend(q, b.k_cache, b.v_cache, bt, sl, qsl, b.scale)
+    assert err.value.code == -4
+
+
 def test_repeated_calls_reuse_workspace(pkvlib):
     b = workload(2, device="cuda")
     meta = to_device(b)
