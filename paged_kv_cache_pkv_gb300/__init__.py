@@ -18,7 +18,7 @@ import os
 import torch
 
 __all__ = [
-    "PkvError", "PkvUnavailable", "lib", "library_path", "Desc", "write", "attend",
+    "PkvError", "PkvUnavailable", "lib", "open_library", "library_path", "Desc", "write", "attend",
     "workspace_size", "get_last_error", "launch_count", "Trace", "PagePool", "KERNELS",
     "export_pages", "import_pages", "write_fp8", "attend_fp8", "workspace_size_fp8",
     "STATUS_BAD_SLOT", "STATUS_BAD_BLOCK", "STATUS_BAD_QUERY", "STATUS_TIMEOUT",
@@ -85,19 +85,26 @@ _SIGS = {
 _lib = None
 
 
+def open_library(path):
+    """A ctypes handle of a build of the library at ``path``, with every
+    entry point's signature declared.  Each build loaded this way keeps its
+    own device status word, launch count and caches."""
+    if not os.path.exists(path):
+        raise PkvUnavailable(
+            f"{path} is missing: build it with "
+            "`python -m paged_kv_cache_pkv_gb300.build` (nvcc, sm_103a)")
+    handle = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(handle, name)
+        fn.restype, fn.argtypes = res, args
+    return handle
+
+
 def lib():
     """The loaded shared library (raises PkvUnavailable if it is not built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(library_path):
-            raise PkvUnavailable(
-                f"{library_path} is missing: build it with "
-                "`python -m paged_kv_cache_pkv_gb300.build` (nvcc, sm_103a)")
-        handle = ctypes.CDLL(library_path)
-        for name, (res, args) in _SIGS.items():
-            fn = getattr(handle, name)
-            fn.restype, fn.argtypes = res, args
-        _lib = handle
+        _lib = open_library(library_path)
     return _lib
 
 

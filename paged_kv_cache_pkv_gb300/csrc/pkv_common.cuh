@@ -46,10 +46,18 @@ __host__ __device__ constexpr int partial_floats(int heads) {
   return kPartialHeader + heads * kHeadDim;
 }
 
-// Bounded waits: a kernel gives up on an mbarrier after this many
-// nanoseconds of polling, flags PKV_STATUS_TIMEOUT and returns.
-constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // 200 ms
+// Bounded waits: a kernel gives up on an mbarrier or a counter after this
+// many nanoseconds of polling, flags PKV_STATUS_TIMEOUT and returns (after
+// letting its own copies and MMAs in flight land, within kDrainLimitNs).
+// The limit is a build option so that a test build can make waits run out.
+#ifndef PKV_WAIT_LIMIT_NS
+#define PKV_WAIT_LIMIT_NS 200000000ull  // 200 ms
+#endif
+constexpr uint64_t kWaitLimitNs = PKV_WAIT_LIMIT_NS;
 constexpr uint64_t kDrainLimitNs = 2ull * 1000 * 1000;   // 2 ms for the clean-up path
+// Waits whose only purpose is to let a CTA's own copies or MMAs land before
+// it releases shared memory or TMEM: never shorter than the drain limit.
+constexpr uint64_t kLandLimitNs = kWaitLimitNs > kDrainLimitNs ? kWaitLimitNs : kDrainLimitNs;
 
 // Shared-prefix partial record: o[128] unnormalised, then m (log2 domain)
 // and l; padded to a 16-byte multiple.
@@ -140,6 +148,32 @@ __device__ __forceinline__ unsigned long long atom_add_acq_rel(unsigned long lon
   unsigned long long old;
   asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
   return old;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Arrival on a counter word that holds a 48-bit launch epoch over a 16-bit
+// count.  The launch stamps (epoch, 0) into the word before any arrival can
+// happen, but the stamp may not be visible yet, and an add that reaches the
+// word before it is overwritten by it.  So: one add (the usual case, the
+// stamp is there); if the word still held an older epoch, plain loads wait
+// for the stamp (bounded) and the add is made again.  No arrival adds twice
+// into an older epoch's word, so with fewer than 32768 arrivals per launch
+// that word's count never carries into its epoch field.  Returns the count
+// before this arrival, or -1 when the stamp did not appear in time.
+__device__ __forceinline__ int arrive_stamped(unsigned long long* ctr, unsigned long long epoch) {
+  unsigned long long v = atom_add_acq_rel(ctr, 1ull);
+  if ((v >> 16) != epoch) {
+    const uint64_t t0 = global_ns();
+    while ((ld_acquire_gpu(ctr) >> 16) != epoch)
+      if (global_ns() - t0 > kWaitLimitNs) return -1;
+    v = atom_add_acq_rel(ctr, 1ull);
+  }
+  return int(v & 0xFFFFull);
 }
 
 // Programmatic dependent launch: wait until the grids this one depends on

@@ -22,9 +22,12 @@
 //    complete on an mbarrier; all 32 lanes compute.  No CTA barrier sits on
 //    the page loop.
 //  * Page products on warp-level MMAs (mma.sync m16n8k16, f32 accumulators)
-//    fed straight from registers: S^T[16 tokens x 8 heads] = K . Q^T, then
-//    O^T[128 dims x 8 heads] += V^T . P^T (the GH <= 4 heads of a group pad
-//    N = 8).  The contraction index of both products is permuted so that
+//    fed straight from registers: S^T[16 tokens x 8 columns] = K . Q^T, then
+//    O^T[128 dims x 8 columns] += V^T . P^T.  Column c < GH is query head c
+//    of the group; column GH + c repeats head c (the same scores) and carries
+//    the rounding remainder of its P, so P enters the PV product as two terms
+//    (rounded value + rounded remainder) at no extra MMA: the flush adds the
+//    two columns.  The contraction index of both products is permuted so that
 //    every lane's operands are whole 16-byte pieces of shared memory: lane
 //    (g, t) reads dims 32t..32t+31 of K rows g and g+8 and dims 16g..16g+15
 //    of V rows 2t, 2t+1, 2t+8, 2t+9.  A tcgen05 MMA needs M >= 64 and its
@@ -32,12 +35,12 @@
 //    operands come from registers, so the warp-level MMA is the fit.  It needs
 //    about a quarter of the instructions of packed FMAs, which lets a CTA run
 //    12 warps (168 registers) and hide more latency.
-//  * bf16 pages: bf16 operands as stored (q too), P rounded to bf16; a page
+//  * bf16 pages: bf16 operands as stored (q too), P as two bf16 terms; a page
 //    is one TMA tensor copy (the pool viewed as rows of 128 bytes, 128-byte
 //    swizzle: conflict-free fragment reads).  FP8 pages (template flag F8):
 //    2 KiB pages of E4M3 codes by the same kind of copy, plus 16-byte blocks
 //    of per-row scale bytes (scale = 2^(byte-127)) by bulk copies; codes are widened exactly to f16 (E4M3 is a subset of f16), q is
-//    scaled by a power of two into f16 range (exact), P is f16.  Row scales:
+//    scaled by a power of two into f16 range (exact), P is two f16 terms.  Row scales:
 //    the K one multiplies the finished score; the V one weights the
 //    probability relative to the largest V scale of the segment (a running
 //    exponent, like the softmax maximum).
@@ -143,6 +146,12 @@ __device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// (a, b) minus their f16 pair `rounded` (exact in fp32), rounded to f16.
+__device__ __forceinline__ uint32_t f16_remainder(uint32_t rounded, float a, float b) {
+  const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&rounded));
+  return pack_f16x2(a - r.x, b - r.y);
 }
 
 // D += A . B, m16n8k16, f16 operands, f32 accumulators (warp-collective).
@@ -450,8 +459,10 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
   // per thread, so that arrivals are single atomic adds.  A counter is first
   // hit when a warp finishes a split item, long after these stamps; an
   // arrival that still sees an old epoch adds again once it is stamped.
+#ifndef PKV_TEST_NO_EPOCH_STAMP  // a test build leaves the counters unstamped: arrivals time out
   for (int i = blockIdx.x * NT + threadIdx.x; i < p.T * per_row; i += gridDim.x * NT)
     atomicExch(p.counters + i, p.epoch << 16);
+#endif
   // the prefill pass launched after this kernel counts its exits here (it
   // launches only once this CTA has passed its trigger below, or exited)
   if (p.lead && blockIdx.x == 0 && threadIdx.x == 0) atomicExch(p.join, p.epoch << 16);
@@ -664,11 +675,12 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
     cur_h0 = g * p.G + sub * GH;
     const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (size_t(d.row) * p.Hq + cur_h0) * kHeadDim);
     if constexpr (!F8) {
-      // bf16 pages: the Q^T operand is q's own bf16 pairs (zero past the group)
+      // bf16 pages: the Q^T operand is q's own bf16 pairs; column gq is head
+      // gq % GH for gq < 2 GH (the remainder columns repeat the heads), zero past
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint4 x = make_uint4(0, 0, 0, 0);
-        if (gq < GH) x = __ldg(qrow + gq * 16 + tq * 4 + c);
+        if (gq < 2 * GH) x = __ldg(qrow + (gq & (GH - 1)) * 16 + tq * 4 + c);
         qb[2 * c][0] = x.x;
         qb[2 * c][1] = x.y;
         qb[2 * c + 1][0] = x.z;
@@ -676,13 +688,13 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
       }
       qmul = p.qscale;
     } else {
-      // head gq's dims 32tq..32tq+31 (zero for heads past the group)
+      // column gq's dims 32tq..32tq+31: head gq % GH for gq < 2 GH, zero past
       float qv[32];
       float amax = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint4 x = make_uint4(0, 0, 0, 0);
-        if (gq < GH) x = __ldg(qrow + gq * 16 + tq * 4 + c);
+        if (gq < 2 * GH) x = __ldg(qrow + (gq & (GH - 1)) * 16 + tq * 4 + c);
         const uint32_t wq[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -718,6 +730,18 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
   // of head h from the lane with tq = h/2 that holds them; par 1 lanes hold 0.
   // l is summed over the lanes of a tq.
   auto frag_to_common = [&]() {
+    // add each remainder column into its head's column: column GH + c sits
+    // in lane tq + GH/2 (GH = 2, 4), or next to column 0 in the same lane
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      if constexpr (GH == 1) {
+        oacc[mb][0] += oacc[mb][1];
+        oacc[mb][2] += oacc[mb][3];
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oacc[mb][e] += __shfl_xor_sync(kFull, oacc[mb][e], GH / 2);
+      }
+    }
     const float os = F8 ? scale_of(uint32_t(eref)) : 1.f;
 #pragma unroll
     for (int h = 0; h < GH; ++h) {
@@ -871,18 +895,10 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
     int last = 0;
     if (lane == 0) {
       const int w0 = cur_item_start / chunk, w1 = (cur_item_start + npages - 1) / chunk;
-      const unsigned long long nparts = static_cast<unsigned long long>(w1 - w0 + 1);
-      unsigned long long* ctr = p.counters + size_t(cur_row) * per_row + cur_item;
-      unsigned long long v = atom_add_acq_rel(ctr, 1ull);
-      const uint64_t t0 = global_ns();
-      while ((v >> 16) != p.epoch) {  // not stamped yet: the stamp overwrites this add
-        if (global_ns() - t0 > kWaitLimitNs) {
-          flag_status(p.status, PKV_STATUS_TIMEOUT);
-          break;
-        }
-        v = atom_add_acq_rel(ctr, 1ull);
-      }
-      last = (v >> 16) == p.epoch && (v & 0xFFFFull) + 1 == nparts;
+      const int nparts = w1 - w0 + 1;
+      const int before = arrive_stamped(p.counters + size_t(cur_row) * per_row + cur_item, p.epoch);
+      if (before < 0) flag_status(p.status, PKV_STATUS_TIMEOUT);  // no merge: the row stays unwritten
+      last = before + 1 == nparts;
     }
     last = __shfl_sync(kFull, last, 0);
     if (last) {
@@ -896,7 +912,9 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
   for (; it < n_units; ++it) {
     const int stage = it % NS;
     const uint32_t parity = (it / NS) & 1;
-    if (!mbar_wait(&M.bar[stage], parity)) {
+    // the warp leaves together (the loop body is warp-collective), even if
+    // the lanes' clocks disagree about the limit
+    if (!__all_sync(kFull, mbar_wait(&M.bar[stage], parity))) {
       timed_out = true;
       break;
     }
@@ -945,7 +963,7 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
       }
       // scores (log2 domain) of tokens gq, gq+8 for heads 2tq, 2tq+1
       const bool t0 = gq < nvalid, t1 = gq + 8 < nvalid;
-      const bool h0 = 2 * tq < GH, h1r = 2 * tq + 1 < GH;
+      const bool h0 = 2 * tq < 2 * GH, h1r = 2 * tq + 1 < 2 * GH;
       uint32_t kb_0, kb_1, vb_0, vb_1;
       bytes_t_t8(ksc, gq, kb_0, kb_1);
       bytes_t_t8(vsc, gq, vb_0, vb_1);
@@ -1021,16 +1039,20 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
         const int dl = int(vb_1) - eref + 127;
         w1 = dl >= 1 ? scale_of(uint32_t(dl)) : 0.f;
       }
-      // this lane's P for its even head (2tq) and odd head (2tq+1): tokens gq, gq+8
-      const uint32_t pe = pack_f16x2(p0 * w0, p2 * w1), po = pack_f16x2(p1 * w0, p3 * w1);
-      // P^T operand: head gq, tokens 2tq, 2tq+1 (b0) and 2tq+8, 2tq+9 (b1),
-      // gathered from the lanes that hold those tokens for head pair gq/2
+      // this lane's P for its even column (2tq) and odd column (2tq+1): tokens
+      // gq, gq+8; a remainder column takes what the f16 rounding dropped
+      const float pw0 = p0 * w0, pw2 = p2 * w1, pw1 = p1 * w0, pw3 = p3 * w1;
+      uint32_t pe = pack_f16x2(pw0, pw2), po = pack_f16x2(pw1, pw3);
+      if (2 * tq >= GH) pe = f16_remainder(pe, pw0, pw2);
+      if (2 * tq + 1 >= GH) po = f16_remainder(po, pw1, pw3);
+      // P^T operand: column gq, tokens 2tq, 2tq+1 (b0) and 2tq+8, 2tq+9 (b1),
+      // gathered from the lanes that hold those tokens for column pair gq/2
       const int src0 = 8 * tq + (gq >> 1), src1 = src0 + 4;
       const uint32_t x0 = __shfl_sync(kFull, pe, src0), x1 = __shfl_sync(kFull, po, src0);
       const uint32_t y0 = __shfl_sync(kFull, pe, src1), y1 = __shfl_sync(kFull, po, src1);
       const uint32_t X = (gq & 1) ? x1 : x0, Y = (gq & 1) ? y1 : y0;
       uint32_t pb0 = __byte_perm(X, Y, 0x5410), pb1 = __byte_perm(X, Y, 0x7632);
-      if (gq >= GH) pb0 = pb1 = 0u;
+      if (gq >= 2 * GH) pb0 = pb1 = 0u;
 
       // ---- O^T += V^T . P^T: 8 M-blocks of 16 (permuted) dims ----
       if (nvalid < kPage) {  // rows past the sequence may hold anything (NaN)
@@ -1091,7 +1113,7 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
         for (int e = 0; e < 4; ++e) sacc[e] += sodd[e];
       }
       const bool t0 = gq < nvalid, t1 = gq + 8 < nvalid;
-      const bool h0 = 2 * tq < GH, h1r = 2 * tq + 1 < GH;
+      const bool h0 = 2 * tq < 2 * GH, h1r = 2 * tq + 1 < 2 * GH;
       float sv[4];
       sv[0] = t0 && h0 ? sacc[0] * qmul : -INFINITY;
       sv[1] = t0 && h1r ? sacc[1] * qmul : -INFINITY;
@@ -1125,14 +1147,17 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
       const float p0 = ex2(sv[0] - r0), p1 = ex2(sv[1] - r1), p2 = ex2(sv[2] - r0), p3 = ex2(sv[3] - r1);
       l2[0] += p0 + p2;
       l2[1] += p1 + p3;
-      const uint32_t pe = pack_bf16x2(p0, p2), po = pack_bf16x2(p1, p3);
-      // P^T operand: head gq, tokens tq, tq+4 (b0) and tq+8, tq+12 (b1)
+      uint32_t pe = pack_bf16x2(p0, p2), po = pack_bf16x2(p1, p3);
+      // remainder columns: p - bf16(p) (exact in fp32), rounded to bf16
+      if (2 * tq >= GH) pe = pack_bf16x2(p0 - bf_lo(pe), p2 - bf_hi(pe));
+      if (2 * tq + 1 >= GH) po = pack_bf16x2(p1 - bf_lo(po), p3 - bf_hi(po));
+      // P^T operand: column gq, tokens tq, tq+4 (b0) and tq+8, tq+12 (b1)
       const int src0 = 4 * tq + (gq >> 1), src1 = src0 + 16;
       const uint32_t x0 = __shfl_sync(kFull, pe, src0), x1 = __shfl_sync(kFull, po, src0);
       const uint32_t y0 = __shfl_sync(kFull, pe, src1), y1 = __shfl_sync(kFull, po, src1);
       const uint32_t X = (gq & 1) ? x1 : x0, Y = (gq & 1) ? y1 : y0;
       uint32_t pb0 = __byte_perm(X, Y, 0x5410), pb1 = __byte_perm(X, Y, 0x7632);
-      if (gq >= GH) pb0 = pb1 = 0u;
+      if (gq >= 2 * GH) pb0 = pb1 = 0u;
 
       // ---- O^T += V^T . P^T (rows past the sequence may hold anything) ----
       if (nvalid < kPage) {
@@ -1316,8 +1341,9 @@ int launch_attend(const LaunchCtx& ctx, const AttendArgs& a) {
   // the prefill pass behind it on the rest.  Otherwise the pass first and
   // split-KV beside it on the SMs it leaves free.
   const int pf_cost = prefill_step_units(a.fp8);
+  // (the pass counts its CTAs' exits on a 16-bit count: fewer than 32768)
   const bool lead = prefill && a.shared_prefix_pages == 0 && pf_cost > 0 &&
-                    int64_t(d.num_kv_heads) * prefill_groups(d, a.num_seqs, a.num_tokens, max_tiles) < 0xFFFF;
+                    int64_t(d.num_kv_heads) * prefill_groups(d, a.num_seqs, a.num_tokens, max_tiles) < 0x8000;
   const unsigned long long epoch = next_epoch();
   unsigned long long* join = reinterpret_cast<unsigned long long*>(ws + L.tiles);
   if (prefill && !lead) {

@@ -26,11 +26,14 @@
 //    the running max in the log2 domain, row max exchanged through shared
 //    memory.  The running max only moves when a score exceeds it by more than
 //    kTau (then the pass is redone and O in TMEM is rescaled), so most tiles
-//    take one pass.  P is rounded to bf16 and stored into TMEM over the
+//    take one pass.  P is stored into TMEM over the
 //    thread's own S columns (two bf16 per 32-bit column, row = lane), where
-//    the PV MMA reads its A operand: no shared-memory traffic for P.
-//  * O += P V: per Q tile 8 tcgen05.mma (A from TMEM) into TMEM columns
-//    256..383 / 384..511; V is the N-major (dims contiguous) operand in shared
+//    the PV MMA reads its A operand: no shared-memory traffic for P.  P goes
+//    in as two bf16 terms, the rounded value and the rounded remainder
+//    (p - bf16(p), exact in fp32), each in half of the thread's 64 S columns,
+//    so the rounding of P costs no accuracy (2^-16 of P instead of 2^-8).
+//  * O += P V: per Q tile 16 tcgen05.mma (A from TMEM; 8 for each term of P)
+//    into TMEM columns 256..383 / 384..511; V is the N-major (dims contiguous) operand in shared
 //    memory.  V rows past the sequence end are zeroed in shared memory first
 //    so stale pool contents cannot reach O.
 //  * Warp roles: warps 0-7 run the softmax of the two Q tiles in turn; warp 8
@@ -118,17 +121,13 @@ struct PrefillParams {
 // split-KV kernel this pass was launched behind.
 __device__ __forceinline__ void join_exit(const PrefillParams& p) {
   if (!p.join) return;
-  const unsigned long long total = static_cast<unsigned long long>(gridDim.x) * gridDim.y;
-  unsigned long long v = atom_add_acq_rel(p.join, 1ull);
-  const uint64_t t0 = global_ns();
-  while ((v >> 16) != p.epoch) {  // not stamped yet: the stamp overwrites this add
-    if (global_ns() - t0 > kWaitLimitNs) {
-      flag_status(p.status, PKV_STATUS_TIMEOUT);
-      return;
-    }
-    v = atom_add_acq_rel(p.join, 1ull);
+  const int total = int(gridDim.x * gridDim.y);  // < 32768 (checked on the host)
+  const int before = arrive_stamped(p.join, p.epoch);
+  if (before < 0) {
+    flag_status(p.status, PKV_STATUS_TIMEOUT);
+    return;
   }
-  if ((v & 0xFFFFull) + 1 == total) griddep_wait();
+  if (before + 1 == total) griddep_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -532,13 +531,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     mbar_arrive_expect_tx(bar, uint32_t(valid) * 2 * 2048);
 #pragma unroll
     for (int j = 0; j < kPfPagesPerTile; ++j) {
-      if (bids[j] < 0) continue;
-      int bid = bids[j];
-      if (bid >= p.num_blocks) {
-        flag_status(p.status, PKV_STATUS_BAD_BLOCK);
-        bid = 0;
-      }
-      const int row = (bid * p.Hkv + g) * kPage;
+      if (bids[j] < 0) continue;  // past the window
+      const int row = (bids[j] * p.Hkv + g) * kPage;
       tma_load_2d(base + j * 2048, map, 0, row, bar);
       tma_load_2d(base + kHalfTile + j * 2048, map, 64, row, bar);
     }
@@ -562,11 +556,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int h = 0; h < 2; ++h)
           tma_load_3d(sQ + (u * 2 + h) * kHalfTile, &tm_q, h * 64, g * p.G, q_tok0 + u * p.TM, bar_q);
     }
-    // lane l: page l % 8 of tile 4 * grp + l / 8 of this CTA's window (-1 past it)
+    // lane l: page l % 8 of tile 4 * grp + l / 8 of this CTA's window; -1
+    // past the window (no copy).  A table entry inside the window that is
+    // not a page of the pool (negative, or num_blocks and up) is flagged and
+    // page 0 is read in its place, so every id returned for a live page is
+    // in the pool.
     auto group_id = [&](int grp) {
       const int kt = grp * 4 + lane / kPfPagesPerTile;
       const int pi = (kbeg + kt) * kPfPagesPerTile + lane % kPfPagesPerTile;
-      return (kt < nkv && pi < npages) ? __ldg(bt_row + pi) : -1;
+      if (kt >= nkv || pi >= npages) return -1;
+      int bid = __ldg(bt_row + pi);
+      if (bid < 0 || bid >= p.num_blocks) {
+        flag_status(p.status, PKV_STATUS_BAD_BLOCK);
+        bid = 0;
+      }
+      return bid;
     };
     int cur_g = group_id(0);
     int next_g = nkv > 4 ? group_id(1) : -1;
@@ -586,10 +590,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_arrive_expect_tx(bar_st, uint32_t(valid) * (kStagePage + kScaleBytes));
     };
     auto stage_page = [&](int j, int bid) {
-      if (bid >= p.num_blocks) {
-        flag_status(p.status, PKV_STATUS_BAD_BLOCK);
-        bid = 0;
-      }
       tma_load_2d(stage + j * kStagePage, map, 0, (bid * p.Hkv + g) * kPage, bar_st);
       bulk_copy(ssc + j * kScaleBytes, scl + (size_t(bid) * p.Hkv + g) * kScaleBytes, kScaleBytes, bar_st);
     };
@@ -664,8 +664,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (lane == 0) {
       // copies land before the CTA's shared memory is released
       for (int k = max(0, loaded - kKVBufs); k < loaded; ++k)
-        mbar_wait(bar_load + k % kKVBufs, (k / kKVBufs) & 1, ok ? kWaitLimitNs : kDrainLimitNs);
-      if (F8 && st_pending >= 0) mbar_wait(bar_st, st_pending & 1, ok ? kWaitLimitNs : kDrainLimitNs);
+        mbar_wait(bar_load + k % kKVBufs, (k / kKVBufs) & 1, ok ? kLandLimitNs : kDrainLimitNs);
+      if (F8 && st_pending >= 0) mbar_wait(bar_st, st_pending & 1, ok ? kLandLimitNs : kDrainLimitNs);
       if (!ok) flag_status(p.status, PKV_STATUS_TIMEOUT);
     }
     __syncwarp();
@@ -701,10 +701,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // P(u, it) written by the softmax; V(it) landed
         if (!(ok = wait_idle(bar_p + u, it & 1) && wait_idle(bar_v + vb, (it / kKVBufs) & 1))) break;
         tc_fence_after();
+        // 16 keys = 8 packed TMEM columns of P; the remainder term of the
+        // same keys sits 32 columns on
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {  // 16 keys = 8 packed TMEM columns of P
-          const uint64_t bdesc = smem_desc(smem_u32(sV + vb * 2 * kHalfTile) + ks * 2048, kHalfTile, 1024);
-          umma_ts(tmem_o(u), tmem_s(u) + (ks >> 2) * 64 + (ks & 3) * 8, bdesc, idesc_o,
+        for (int ks = 0; ks < 16; ++ks) {
+          const int k16 = ks & 7;
+          const uint64_t bdesc = smem_desc(smem_u32(sV + vb * 2 * kHalfTile) + k16 * 2048, kHalfTile, 1024);
+          umma_ts(tmem_o(u), tmem_s(u) + (k16 >> 2) * 64 + (ks >> 3) * 32 + (k16 & 3) * 8, bdesc, idesc_o,
                   (it > 0 || ks > 0) ? 1u : 0u);
         }
         umma_commit(bar_o + u);
@@ -716,12 +719,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           ++ns;
         }
       }
-      if (!ok) {
-        flag_status(p.status, PKV_STATUS_TIMEOUT);
-        // this lane's newest commits land before TMEM is released
-        if (ns > 0) mbar_wait(bar_s + u, (ns - 1) & 1, kDrainLimitNs);
-        if (npv > 0) mbar_wait(bar_o + u, (npv - 1) & 1, kDrainLimitNs);
-      }
+      if (!ok) flag_status(p.status, PKV_STATUS_TIMEOUT);
+      // this lane's newest commits land before TMEM is released, whatever
+      // the softmax threads' waits saw (each commit covers every earlier MMA
+      // of this lane, and at most one phase of either barrier is pending)
+      if (ns > 0) mbar_wait(bar_s + u, (ns - 1) & 1, ok ? kLandLimitNs : kDrainLimitNs);
+      if (npv > 0) mbar_wait(bar_o + u, (npv - 1) & 1, ok ? kLandLimitNs : kDrainLimitNs);
     }
     __syncwarp();
   } else {
@@ -741,8 +744,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // running max (same in both threads of a row) and half row sum, per tile
     float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
     float* s_red = reinterpret_cast<float*>(sm + kOffM + 256);  // [2][128] exchange
-    bool ok = true;
-    for (int it = 0; it < nkv && ok; ++it) {
+    // ok: this thread's waits all succeeded.  stop: some softmax thread's
+    // failed, decided at the same barrier by all 256 of them, so they leave
+    // the loop together (the loop holds named barriers).
+    bool ok = true, stop = false;
+    for (int it = 0; it < nkv && !stop; ++it) {
       for (int u = 0; u < nt; ++u) {
         const int ph = it & 1;
         const int posu = u ? pos[1] : pos[0];
@@ -755,7 +761,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // runs warp-collective TMEM loads, so the choice must be warp-uniform
         const bool full = __all_sync(0xffffffffu, kbase + 63 <= posu);
         const uint32_t scol = tmem_s(u) + lane_off + ch * 64;
-        uint32_t pk[2][16];
+        uint32_t pk[2][16], pl[2][16];  // P as bf16 pairs, and the rounding remainders
         float mx = -INFINITY, rs = 0.f;
         // One pass over the 64 columns: exp2(s*scale - mref) packed to bf16,
         // optionally tracking the raw maximum.  FULL: no key of this half tile
@@ -785,6 +791,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               const float a1 = ex2(fmaf(x1, p.qscale, -mref));
               acc[e & 3] += a0 + a1;
               pk[c][e] = pack_bf16x2(a0, a1);
+              pl[c][e] = pack_bf16x2(a0 - bf_lo(pk[c][e]), a1 - bf_hi(pk[c][e]));
             }
           }
           rs = (acc[0] + acc[1]) + (acc[2] + acc[3]);
@@ -799,6 +806,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // softmax thread here, together
         if (named_sync_or(2, kPfSoftmaxThreads, !ok)) {
           ok = false;
+          stop = true;
           break;
         }
         const bool grow = row_mx > m + kPfTau;
@@ -824,9 +832,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           l0 = l0 * alpha + rs;
         }
         // P (bf16 pairs) over this thread's own S columns: row r, keys
-        // ch*64 .. ch*64+63 = 32 columns from the start of its half.  The
-        // other thread of the row may still read its S half; this one is done
-        // with its own.
+        // ch*64 .. ch*64+63 = 32 columns from the start of its half, and
+        // their remainders in the next 32.  The other thread of the row may
+        // still read its S half; this one is done with its own.
         {
           uint32_t pw[32];
 #pragma unroll
@@ -835,6 +843,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             pw[16 + e] = pk[1][e];
           }
           tmem_st32(scol, pw);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            pw[e] = pl[0][e];
+            pw[16 + e] = pl[1][e];
+          }
+          tmem_st32(scol + 32, pw);
           tmem_wait_st();
         }
         // rescale this thread's 64 O columns when the running max moved; O is

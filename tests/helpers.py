@@ -51,3 +51,29 @@ def compare(out_gpu: torch.Tensor, expected: np.ndarray, rows=None, what=""):
     mx, mean = float(err.max()), float(err.mean())
     assert mx <= MAX_ABS_TOL and mean <= MEAN_ABS_TOL, f"{what}: max {mx:.3e} mean {mean:.3e}"
     return mx, mean
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Finite float64 values rounded to bf16 (through float32; ties to even),
+    returned as float64."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def compare_large_outputs(out_gpu: torch.Tensor, expected: np.ndarray, rows=None, what=""):
+    """Outputs of magnitude 2..4, where bf16 values are 2^-6 apart.  The max
+    bar stays 1e-2.  No bf16 result can have a mean error below that of the
+    exact result rounded to bf16 (about 2^-8 here, four times the 1e-3 bar
+    set for N(0, 1) data), so the mean bar is that floor plus 2e-4."""
+    got = O.bf16_to_f64(bits(out_gpu))
+    if rows is not None:
+        got, expected = got[rows], expected[rows]
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got - expected)
+    floor = float(np.abs(round_to_bf16(expected) - expected).mean())
+    mx, mean = float(err.max()), float(err.mean())
+    assert np.abs(expected).min() >= 1.99, f"{what}: outputs are not all large"
+    assert mx <= MAX_ABS_TOL and mean <= floor + 2e-4, \
+        f"{what}: max {mx:.3e} mean {mean:.3e} (rounding floor {floor:.3e})"
+    return mx, mean

@@ -15,8 +15,8 @@ import torch
 
 import oracle.pkv_oracle as O
 import paged_kv_cache_pkv_gb300 as pkv
-from helpers import bits, compare, oracle_attend, oracle_write, to_device
-from workloads import make_batch, workload
+from helpers import bits, compare, compare_large_outputs, oracle_attend, oracle_write, to_device
+from workloads import large_value_rows, make_batch, workload
 
 pytestmark = pytest.mark.gpu
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -170,10 +170,9 @@ def test_query_longer_than_sequence_is_flagged(pkvlib):
 def test_most_sequences_per_call(pkvlib):
     """PKV_MAX_SEQS decode sequences in one call fill the plan's per-sequence
     arrays in shared memory: every row against the oracle; one more sequence
-    is a range error.  32-64 keys per row: with only a few keys an output is
-    close to one V row (|out| near 4 on this data), where the bf16 output
-    rounding alone uses 7.8e-3 of the 1e-2 budget."""
-    lens = np.random.default_rng(2048).integers(32, 65, size=2048).tolist()
+    is a range error.  1-64 keys per row: with only a few keys an output is
+    close to one V row (|out| near 4 on this data)."""
+    lens = np.random.default_rng(2048).integers(1, 65, size=2048).tolist()
     b = make_batch(lens, [1] * 2048, 8, 2, seed=2048, device="cuda")
     check_batch(b, what="2048 sequences")
     meta = to_device(b)
@@ -345,3 +344,75 @@ def test_cascade_row_without_own_key_is_flagged(pkvlib):
     pkv.attend(b.q, kc, vc, meta["block_tables"], meta["seq_lens"], meta["query_start_loc"], b.scale,
                max_query_len=1, shared_prefix_pages=10)
     assert pkv.get_last_error() & pkv.STATUS_BAD_QUERY
+
+
+# Outputs of magnitude 2..3.875, where bf16 values are 2^-6 apart: the output
+# rounding alone may cost 7.8e-3 of the 1e-2 budget, so P must not add a
+# rounding of its own (one bf16 rounding of P moves an output by up to 2^-8
+# of the V rows it weighs).  Rows with few keys have the least averaging.
+
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (16, 8), (8, 8), (64, 8)])
+def test_short_decode_rows_with_large_outputs(pkvlib, hq, hkv):
+    """Decode rows over 1-24 keys, every output element in [2, 3.875] in
+    magnitude; query-head groups of 4, 2 and 1 (the page product's
+    remainder columns sit differently for each) and 8 (two groups)."""
+    lens = np.random.default_rng(hq).integers(1, 25, size=768).tolist()
+    b = large_value_rows(make_batch(lens, [1] * len(lens), hq, hkv, seed=500 + hq, device="cuda"), 600 + hq)
+    out, _, _ = run_step(b)
+    assert pkv.get_last_error() == 0
+    k_ref, v_ref = oracle_write(b)
+    compare_large_outputs(out, oracle_attend(b, k_ref, v_ref), what=f"short rows, large outputs {hq}/{hkv}")
+
+
+@pytest.mark.parametrize("hq,hkv,chunks", [(32, 8, [300, 200]), (8, 8, [260]), (16, 2, [129, 64])])
+def test_prefill_from_position_zero_with_large_outputs(pkvlib, hq, hkv, chunks):
+    """Chunks that start at position 0 (L = n: query j sees keys 0..j, so the
+    first rows see one, two, three keys) on the tensor-core kernel, with
+    every output element in [2, 3.875] in magnitude, next to a decode row."""
+    lens = chunks + [40]
+    b = large_value_rows(make_batch(lens, chunks + [1], hq, hkv, seed=700 + sum(chunks), device="cuda"),
+                         800 + hq)
+    counts, out, _, _ = _kernel_launches(b, max(chunks))
+    assert counts["prefill"] == 1
+    assert pkv.get_last_error() == 0
+    k_ref, v_ref = oracle_write(b)
+    compare_large_outputs(out, oracle_attend(b, k_ref, v_ref), what=f"prefill from 0, large outputs {hq}/{hkv}")
+
+
+def test_prefill_bad_block_ids_are_flagged(pkvlib):
+    """Table entries inside a prefill chunk's key window that are not pool
+    pages (negative, and past the pool) are flagged, and page 0 is read in
+    their place; the other sequences' rows are unaffected."""
+    b = make_batch([600, 300, 50], [200, 100, 1], 32, 8, seed=901, device="cuda")
+    meta = to_device(b)
+    meta["block_tables"][0, 3] = -5
+    meta["block_tables"][0, 20] = b.num_blocks + 7
+    pkv.get_last_error()
+    kc, vc = b.k_cache.clone(), b.v_cache.clone()
+    pkv.write(b.k_new, b.v_new, meta["slot_mapping"], kc, vc)
+    tr = pkv.Trace(16)
+    with tr:
+        out = pkv.attend(b.q, kc, vc, meta["block_tables"], meta["seq_lens"], meta["query_start_loc"],
+                         b.scale, max_query_len=200)
+    torch.cuda.synchronize()
+    assert tr.read("prefill")[1] == 1
+    tr.close()
+    assert pkv.get_last_error() & pkv.STATUS_BAD_BLOCK
+    k_ref, v_ref = oracle_write(b)
+    rows = list(range(200, b.T))  # sequences 1 and 2
+    compare(out, oracle_attend(b, k_ref, v_ref, rows=rows), rows=rows, what="rows beside bad block ids")
+
+
+def test_cascade_bad_prefix_block_id_is_flagged(pkvlib):
+    """A negative id among the shared prefix pages reaches the prefix pass's
+    loaders, which flag it."""
+    b = make_batch([512 + 30, 512 + 9], [1, 1], 32, 8, seed=902, device="cuda", pool_factor=1.0,
+                   shared_prefix_tokens=512)
+    meta = to_device(b)
+    meta["block_tables"][:, 5] = -1
+    pkv.get_last_error()
+    kc, vc = b.k_cache.clone(), b.v_cache.clone()
+    pkv.attend(b.q, kc, vc, meta["block_tables"], meta["seq_lens"], meta["query_start_loc"], b.scale,
+               max_query_len=1, shared_prefix_pages=32)
+    torch.cuda.synchronize()
+    assert pkv.get_last_error() & pkv.STATUS_BAD_BLOCK

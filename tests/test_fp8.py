@@ -9,8 +9,8 @@ import torch
 
 import oracle.pkv_oracle as O
 import paged_kv_cache_pkv_gb300 as pkv
-from helpers import bits, compare, to_device
-from workloads import fp8_pools, make_batch, workload
+from helpers import bits, compare, compare_large_outputs, to_device
+from workloads import fp8_pools, large_value_rows, make_batch, workload
 
 pytestmark = pytest.mark.gpu
 
@@ -34,8 +34,8 @@ def _oracle_write(batch, pools, k_new=None, v_new=None):
     return O.write_fp8(kn, vn, batch.slot_mapping, *(_u8(p) for p in pools), batch.page_size)
 
 
-def _run(batch, seed, rows=None, what=""):
-    pools = fp8_pools(batch, seed)
+def _run(batch, seed, rows=None, what="", v_values=None, cmp=compare):
+    pools = fp8_pools(batch, seed, v_values=v_values)
     meta = to_device(batch)
     kc, vc, ks, vs = _gpu_write(batch, pools, meta)
     out = pkv.attend_fp8(batch.q, kc, vc, ks, vs, meta["block_tables"], meta["seq_lens"],
@@ -48,7 +48,7 @@ def _run(batch, seed, rows=None, what=""):
     expected = O.attend_fp8(bits(batch.q), *ref, batch.block_tables, batch.seq_lens,
                             batch.query_start_loc, batch.scale, batch.num_q_heads,
                             batch.num_kv_heads, batch.page_size, rows=rows)
-    return compare(out, expected, rows=rows, what=what or batch.name)
+    return cmp(out, expected, rows=rows, what=what or batch.name)
 
 
 # ---------------------------------------------------------------- write
@@ -330,3 +330,46 @@ def test_attend_fp8_rejects_bad_arguments(pkvlib):
     a[15] = short
     assert lib.pkv_attend_fp8(*a) == -5  # PKV_ERR_WORKSPACE
     torch.cuda.synchronize()
+
+
+# Outputs of magnitude 2..3.875 (bf16 spacing 2^-6): the P of the FP8 paths
+# (f16 in split-KV, bf16 in the tensor-core kernel) must not add a rounding
+# of its own.  The pool's V codes and this step's new V rows both stand for
+# such values.
+
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (16, 8), (8, 8)])
+def test_attend_fp8_short_decode_rows_with_large_outputs(pkvlib, hq, hkv):
+    lens = np.random.default_rng(hq + 1).integers(1, 25, size=768).tolist()
+    b = large_value_rows(make_batch(lens, [1] * len(lens), hq, hkv, seed=520 + hq, device="cuda"), 620 + hq)
+    _run(b, 720 + hq, v_values=b.v_cache, what=f"fp8 short rows, large outputs {hq}/{hkv}",
+         cmp=compare_large_outputs)
+
+
+@pytest.mark.parametrize("hq,hkv,chunks", [(32, 8, [300, 200]), (8, 8, [260])])
+def test_attend_fp8_prefill_from_position_zero_with_large_outputs(pkvlib, hq, hkv, chunks):
+    b = large_value_rows(make_batch(chunks + [40], chunks + [1], hq, hkv, seed=740 + sum(chunks),
+                                    device="cuda"), 840 + hq)
+    _run(b, 760 + hq, v_values=b.v_cache, what=f"fp8 prefill from 0, large outputs {hq}/{hkv}",
+         cmp=compare_large_outputs)
+
+
+def test_attend_fp8_prefill_bad_block_ids_are_flagged(pkvlib):
+    """The FP8 prefill loaders stage pages by block id: ids inside the key
+    window that are not pool pages are flagged and page 0 is staged instead;
+    the other sequences' rows are unaffected."""
+    b = make_batch([600, 300, 50], [200, 100, 1], 32, 8, seed=903, device="cuda")
+    pools = fp8_pools(b, 904)
+    meta = to_device(b)
+    kc, vc, ks, vs = _gpu_write(b, pools, meta)
+    meta["block_tables"][0, 3] = -5
+    meta["block_tables"][0, 20] = b.num_blocks + 7
+    pkv.get_last_error()
+    out = pkv.attend_fp8(b.q, kc, vc, ks, vs, meta["block_tables"], meta["seq_lens"],
+                         meta["query_start_loc"], b.scale, max_query_len=200)
+    torch.cuda.synchronize()
+    assert pkv.get_last_error() & pkv.STATUS_BAD_BLOCK
+    ref = _oracle_write(b, pools)
+    rows = list(range(200, b.T))
+    expected = O.attend_fp8(bits(b.q), *ref, b.block_tables, b.seq_lens, b.query_start_loc, b.scale,
+                            b.num_q_heads, b.num_kv_heads, b.page_size, rows=rows)
+    compare(out, expected, rows=rows, what="fp8 rows beside bad block ids")

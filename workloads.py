@@ -184,26 +184,53 @@ def workload(idx, *, device="cpu", with_tensors=True):
     return b
 
 
+def large_value_rows(batch: Batch, seed: int, lo: float = 2.0, hi: float = 3.875):
+    """Rewrite V (the pre-filled pool and this step's new rows) in place:
+    every element gets a sign fixed per (kv head, dim) and a magnitude
+    uniform in [lo, hi], rounded to bf16.  Any convex combination of such
+    rows (an attention output) then has magnitude in [lo, hi]: with the
+    defaults that is [2, 3.875], where bf16 values are 2^-6 apart, the
+    hardest range for an absolute tolerance of 1e-2.  Values come from a
+    torch.Generator seeded with ``seed`` on the batch's device."""
+    dev = batch.v_cache.device
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    hkv, d = batch.num_kv_heads, batch.head_dim
+    sign = torch.randint(0, 2, (hkv, d), generator=gen, device=dev).to(torch.float32) * 2 - 1
+
+    def draw(shape, sgn):
+        mag = lo + (hi - lo) * torch.rand(shape, generator=gen, device=dev, dtype=torch.float32)
+        return (mag * sgn).to(torch.bfloat16)
+
+    batch.v_cache = draw(tuple(batch.v_cache.shape), sign[None, :, None, :])
+    batch.v_new = draw(tuple(batch.v_new.shape), sign[None, :, :])
+    return batch
+
+
 # Scale byte of the pre-filled FP8 pool: 2^(121 - 127) = 1/64.
 FP8_FILL_SCALE_BYTE = 121
 
 
-def fp8_pools(batch: Batch, seed: int):
+def fp8_pools(batch: Batch, seed: int, v_values: torch.Tensor = None):
     """A pre-filled FP8 page pool for ``batch``: E4M3 codes [NB, Hkv, P, D]
     (uint8) of N(0, 1) * 64 values (clipped to the format's +-448, which
     N(0, 1) reaches only beyond 7 sigma) and a constant scale byte
     FP8_FILL_SCALE_BYTE [NB, Hkv, P] (uint8), so the pool holds values close
     to N(0, 1).  Codes come from torch's float8_e4m3fn conversion with a
-    torch.Generator seeded with ``seed``, on the batch's device.  No per-row
-    scaling: that is the write step's arithmetic, done only by the write
-    under test.  Returns (k_codes, v_codes, k_scale, v_scale)."""
+    torch.Generator seeded with ``seed``, on the batch's device.  With
+    ``v_values`` (a pool-shaped tensor of magnitudes below 7) the V codes
+    stand for those values times 64 instead.  No per-row scaling: that is
+    the write step's arithmetic, done only by the write under test.
+    Returns (k_codes, v_codes, k_scale, v_scale)."""
     dev = batch.q.device if batch.q is not None else torch.device("cpu")
     gen = torch.Generator(device=dev)
     gen.manual_seed(seed)
     shape = (batch.num_blocks, batch.num_kv_heads, batch.page_size, batch.head_dim)
     out = []
-    for _ in range(2):
+    for i in range(2):
         x = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32) * 64.0
+        if i == 1 and v_values is not None:
+            x = v_values.to(device=dev, dtype=torch.float32) * 64.0
         out.append(x.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8))
     sc = torch.full(shape[:3], FP8_FILL_SCALE_BYTE, dtype=torch.uint8, device=dev)
     return out[0], out[1], sc, sc.clone()
