@@ -1231,20 +1231,20 @@ int decode_ctas_per_sm(int variant, bool fp8) {
 
 // Split-KV units (one page of one kv head, K and V) the whole GPU streams
 // while one SM runs one K/V tile step of the prefill pass: bf16 pages about
-// 2.4 us per step (two Q tiles) against 6.5 TB/s / 8 KiB per unit.  Sizes the
-// SM share the split-KV kernel leaves the pass when the pass runs behind it;
-// 0 puts the pass first instead.  Measured on the 96-row mixed step (two
-// 512-token chunks; 2,880 steps against 188,544 units): bf16 1200 / 1900 /
-// 2800 -> 19 / 30 / 43 SMs for the pass -> 278 / 269 / 272 us (pass first:
-// 306 us).  FP8 pages (the pass widens codes, about 5.6 us a step, and
-// split-KV is bound by issue, so the SMs are split in proportion): 46 / 76
-// SMs for the pass -> 342 / 319 us (pass first: 340 us); 10000 gives 77.
+// 3.1 us per step (two Q tiles, P as two terms) against 6.5 TB/s / 8 KiB per
+// unit.  Sizes the SM share the split-KV kernel leaves the pass when the
+// pass runs behind it; 0 puts the pass first instead.  Measured on the
+// 96-row mixed step (two 512-token chunks; 2,880 steps against 188,544
+// units): bf16 1900 / 2300 / 2600 / 3000 -> 298 / 270 / 271 / 271 us.  FP8
+// pages (the pass widens codes, about 5.8 us a step, and split-KV is bound
+// by issue, so the SMs are split in proportion): 10000 / 12500 / 15000 ->
+// 326 / 361 / 398 us (pass first: 340 us).
 static int prefill_step_units(bool fp8) {
   static int v[2] = {-1, -1};
   int& x = v[fp8 ? 1 : 0];
   if (x < 0) {
     const char* e = getenv(fp8 ? "PKV_PREFILL_STEP_UNITS_FP8" : "PKV_PREFILL_STEP_UNITS");
-    x = e ? atoi(e) : (fp8 ? 10000 : 1900);
+    x = e ? atoi(e) : (fp8 ? 10000 : 2400);
   }
   return x;
 }

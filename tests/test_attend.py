@@ -65,22 +65,27 @@ def test_named_workload_all_rows(pkvlib, idx):
     check_batch(workload(idx, device="cuda"))
 
 
-def test_long_tail_sampled_rows(pkvlib):
+def long_tail_rows(b, n=64, seed=0):
+    """The ten longest rows of the long-tail batch (the widest splits), the
+    shortest, and random others: ``n`` rows in all."""
+    order = np.argsort(b.seq_lens, kind="stable")
+    pick = set(order[-10:].tolist()) | {int(order[0])}
+    rest = [r for r in range(b.B) if r not in pick]
+    pick |= set(np.random.default_rng(seed).choice(rest, n - len(pick), replace=False).tolist())
+    return sorted(pick)
+
+
+def test_long_tail_rows(pkvlib):
     b = workload(3, device="cuda")
-    lens = b.seq_lens
-    rng = np.random.default_rng(0)
-    rows = sorted(set([int(np.argmin(lens)), int(np.argmax(lens))] + rng.choice(b.B, 14, replace=False).tolist()))
-    check_batch(b, rows=rows, what="cfg3 sampled")
+    check_batch(b, rows=long_tail_rows(b), what="cfg3 64 rows")
 
 
-def test_mixed_step_sampled_rows(pkvlib):
+def test_mixed_step_all_rows(pkvlib):
+    """Every one of the 1,120 rows: 96 decode rows on split-KV and both
+    512-row chunks on the tensor-core pass running beside it."""
     b = workload(5, device="cuda")
-    qsl = b.query_start_loc
-    pre = [96, 97, 100, 127, 128, 300, 511 + 96, 96 + 512, 96 + 513, 96 + 700, 96 + 1023]
-    rng = np.random.default_rng(1)
-    rows = sorted(set(pre + rng.choice(96, 8, replace=False).tolist()))
-    assert qsl[-1] == 1120
-    check_batch(b, rows=rows, what="cfg5 sampled")
+    assert b.query_start_loc[-1] == 1120
+    check_batch(b, what="cfg5 all rows")
 
 
 @pytest.mark.parametrize("seed", range(6))

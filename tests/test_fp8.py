@@ -119,21 +119,17 @@ def test_attend_fp8_named_all_rows(pkvlib, idx):
     _run(workload(idx, device="cuda"), 90 + idx)
 
 
-def test_attend_fp8_long_tail_sampled_rows(pkvlib):
+def test_attend_fp8_long_tail_rows(pkvlib):
+    from test_attend import long_tail_rows
     b = workload(3, device="cuda")
-    rng = np.random.default_rng(3)
-    rows = sorted(set([int(np.argmin(b.seq_lens)), int(np.argmax(b.seq_lens))]
-                      + rng.choice(b.B, 10, replace=False).tolist()))
-    _run(b, 93, rows=rows, what="cfg3 fp8 sampled")
+    _run(b, 93, rows=long_tail_rows(b, seed=3), what="cfg3 fp8 64 rows")
 
 
-def test_attend_fp8_mixed_step_sampled_rows(pkvlib):
-    """Prefill chunks of 512 rows on the tensor-core kernel, decode rows on
-    split-KV, FP8 pages."""
+def test_attend_fp8_mixed_step_all_rows(pkvlib):
+    """Every row: prefill chunks of 512 rows on the tensor-core kernel,
+    decode rows on split-KV, FP8 pages."""
     b = workload(5, device="cuda")
-    rng = np.random.default_rng(5)
-    rows = sorted(set([96, 97, 300, 96 + 511, 96 + 512, 96 + 1023] + rng.choice(96, 6, replace=False).tolist()))
-    _run(b, 95, rows=rows, what="cfg5 fp8 sampled")
+    _run(b, 95, what="cfg5 fp8 all rows")
 
 
 @pytest.mark.parametrize("seed", range(4))
@@ -252,10 +248,8 @@ def test_attend_fp8_cascade_prefix_shared_workload(pkvlib):
     """Config 4 on FP8 pages: 128 sequences on one 2048-token prefix, the
     prefix attended once per kv head by the tensor-core prefix pass."""
     b = workload(4, device="cuda")
-    rng = np.random.default_rng(4)
-    rows = sorted(rng.choice(b.T, 24, replace=False).tolist())
-    out, expected = _cascade_fp8(b, b.info["shared_prefix_pages"], 97, max_query_len=1, rows=rows)
-    compare(out, expected, rows=rows, what="fp8 cascade cfg4")
+    out, expected = _cascade_fp8(b, b.info["shared_prefix_pages"], 97, max_query_len=1)
+    compare(out, expected, what="fp8 cascade cfg4 all rows")
 
 
 @pytest.mark.parametrize("hq,hkv,prefix,suffixes", [
