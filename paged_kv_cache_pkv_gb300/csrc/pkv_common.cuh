@@ -95,6 +95,16 @@ inline WorkspaceLayout workspace_layout(int num_tokens, int counters_per_row, in
   return w;
 }
 
+// A test build (PKV_TEST_DROP_FIRST_COPY) arms the barrier of a warp's first
+// page (split-KV) and of a CTA's Q tiles (prefill) but issues no copy into
+// it: the waits on those barriers run out, which exercises every timeout
+// path.  Never defined in the library's normal build.
+#ifdef PKV_TEST_DROP_FIRST_COPY
+constexpr bool kDropFirstCopy = true;
+#else
+constexpr bool kDropFirstCopy = false;
+#endif
+
 // ---------------------------------------------------------------------------
 // PTX helpers
 // ---------------------------------------------------------------------------

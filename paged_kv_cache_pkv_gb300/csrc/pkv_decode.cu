@@ -603,6 +603,7 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
       const size_t ph = size_t(pc.bid) * p.Hkv + g;  // (page, kv head)
       M.desc[stage] = StageDesc{pc.q0 + pc.j, pc.item, pc.item_start, pc.nvis - p.np * kPage};
       mbar_arrive_expect_tx(&M.bar[stage], 2 * PB + (F8 ? 2 * kScaleBytes : 0));
+      if (kDropFirstCopy && pc.item_start + pc.page == u_begin) return;
       // one box per page: the pool viewed as [units][128 bytes]; the host
       // checks that unit indices fit int32
       const int unit0 = int(ph) * (PB / 128);

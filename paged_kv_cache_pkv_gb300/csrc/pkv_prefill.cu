@@ -552,7 +552,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (role == 0 && lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
       mbar_arrive_expect_tx(bar_q, uint32_t(nt) * 2 * kHalfTile);
-      for (int u = 0; u < nt; ++u)
+      for (int u = 0; u < (kDropFirstCopy ? 0 : nt); ++u)
         for (int h = 0; h < 2; ++h)
           tma_load_3d(sQ + (u * 2 + h) * kHalfTile, &tm_q, h * 64, g * p.G, q_tok0 + u * p.TM, bar_q);
     }

@@ -2,14 +2,16 @@
 its own copies and MMAs land, frees its TMEM and returns, and the device stays
 usable.
 
-Two test builds of the library, compiled beside the main one and loaded next
-to it (each keeps its own status word):
-  * a wait limit of 1 us: the first waits for pages, Q tiles and MMAs run out
-    long before the copies land, in split-KV, in the tensor-core prefill pass
-    and in the FP8 loaders that widen pages;
-  * a limit of 2 ms with the arrival counters left unstamped (a stamp that
-    nothing writes): every arrival of a split (row, head group) waits for the
-    stamp until the limit.
+Two test builds of the library with a wait limit of 2 ms, compiled beside the
+main one and loaded next to it (each keeps its own status word), each with a
+wait on something that nothing completes:
+  * the first page copy of every split-KV warp and the Q tiles of every
+    prefill CTA are armed on their barriers but never issued: split-KV warps,
+    the prefill pass's MMA, softmax and loader warps (bf16 pages and the FP8
+    loaders that widen pages) all see waits run out, drain what they did
+    issue, free TMEM and return;
+  * the arrival counters are left unstamped: every arrival of a split
+    (row, head group) waits for the stamp until the limit.
 After each, a normal call of the main library on the same stream must still
 match the oracle.  No wait is unbounded, so nothing here can hang the GPU.
 """
@@ -37,8 +39,8 @@ def _test_build(name, flags):
 
 
 @pytest.fixture(scope="module")
-def short_wait_lib(pkvlib):
-    return _test_build("wait1us", ["-DPKV_WAIT_LIMIT_NS=1000ull"])
+def dropped_copy_lib(pkvlib):
+    return _test_build("dropcopy", ["-DPKV_WAIT_LIMIT_NS=2000000ull", "-DPKV_TEST_DROP_FIRST_COPY"])
 
 
 @pytest.fixture(scope="module")
@@ -98,28 +100,29 @@ def _written(b):
 
 
 @pytest.mark.parametrize("batch", ["decode", "mixed"])
-def test_short_mbarrier_waits_run_out_and_return(short_wait_lib, batch):
+def test_dropped_copy_waits_run_out_and_return(dropped_copy_lib, batch):
     torch.cuda.set_device(0)
     if batch == "decode":
         b, mql = workload(2, device="cuda"), 1
     else:  # split-KV first, the tensor-core prefill pass behind it
         b, mql = make_batch([2048, 1000, 300, 64], [512, 200, 1, 1], 32, 8, seed=950, device="cuda"), 512
     meta, kc, vc = _written(b)
-    _flags(short_wait_lib)
-    _attend_with(short_wait_lib, b, meta, kc, vc, max_query_len=mql)
-    assert _flags(short_wait_lib) & pkv.STATUS_TIMEOUT
+    _flags(dropped_copy_lib)
+    out = _attend_with(dropped_copy_lib, b, meta, kc, vc, max_query_len=mql)
+    assert _flags(dropped_copy_lib) & pkv.STATUS_TIMEOUT
+    assert torch.isnan(out.float()).any()  # rows whose first page never came stay unwritten
     _main_library_still_correct(b, meta, kc, vc, max_query_len=mql)
 
 
-def test_short_waits_run_out_in_the_fp8_loaders(short_wait_lib):
+def test_dropped_copy_waits_run_out_in_the_fp8_loaders(dropped_copy_lib):
     torch.cuda.set_device(0)
     b = make_batch([1500, 700, 90], [300, 1, 1], 32, 8, seed=951, device="cuda")
     meta = to_device(b)
     kc, vc, ks, vs = (t.clone() for t in fp8_pools(b, 952))
     pkv.write_fp8(b.k_new, b.v_new, meta["slot_mapping"], kc, vc, ks, vs)
-    _flags(short_wait_lib)
-    _attend_with(short_wait_lib, b, meta, kc, vc, max_query_len=300, fp8_scales=(ks, vs))
-    assert _flags(short_wait_lib) & pkv.STATUS_TIMEOUT
+    _flags(dropped_copy_lib)
+    _attend_with(dropped_copy_lib, b, meta, kc, vc, max_query_len=300, fp8_scales=(ks, vs))
+    assert _flags(dropped_copy_lib) & pkv.STATUS_TIMEOUT
     meta2, kc2, vc2 = _written(b)
     _main_library_still_correct(b, meta2, kc2, vc2, max_query_len=300)
 
