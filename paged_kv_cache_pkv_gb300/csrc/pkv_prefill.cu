@@ -227,6 +227,38 @@ __device__ __forceinline__ bool named_sync_or(int id, int threads, bool flag) {
   return res != 0;
 }
 
+// Packed pairs of fp32 (element 0 in the low word) and the sm_100-family
+// instructions that work on both lanes of a pair at once.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// Largest of three (NaN operands ignored, like fmaxf).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -766,10 +798,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // One pass over the 64 columns: exp2(s*scale - mref) packed to bf16,
         // optionally tracking the raw maximum.  FULL: no key of this half tile
         // is past the row's position (no masking work at all).
+        // Key pairs go through packed fp32 instructions: one FMA for both
+        // exponent arguments, one add into the pair of row sums, one
+        // subtract for both remainders.
         auto pass = [&](float mref, auto full_t, auto track_t) {
           constexpr bool FULL = decltype(full_t)::value, TRACK = decltype(track_t)::value;
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          float mxl[2] = {-INFINITY, -INFINITY};
+          const uint64_t qs2 = f2(p.qscale, p.qscale), nm2 = f2(-mref, -mref);
+          uint64_t acc2[2] = {0ull, 0ull};  // (0, 0) pairs
+          float mxl = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t sv[32];
@@ -783,19 +819,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 if (k > posu) x0 = -INFINITY;
                 if (k + 1 > posu) x1 = -INFINITY;
               }
-              if constexpr (TRACK) {
-                mxl[0] = fmaxf(mxl[0], x0);
-                mxl[1] = fmaxf(mxl[1], x1);
-              }
-              const float a0 = ex2(fmaf(x0, p.qscale, -mref));  // exp2(-inf) = 0
-              const float a1 = ex2(fmaf(x1, p.qscale, -mref));
-              acc[e & 3] += a0 + a1;
-              pk[c][e] = pack_bf16x2(a0, a1);
-              pl[c][e] = pack_bf16x2(a0 - bf_lo(pk[c][e]), a1 - bf_hi(pk[c][e]));
+              if constexpr (TRACK) mxl = max3(mxl, x0, x1);
+              float t0, t1;
+              f2_split(f2_fma(f2(x0, x1), qs2, nm2), t0, t1);
+              const float a0 = ex2(t0), a1 = ex2(t1);  // exp2(-inf) = 0
+              const uint64_t a2 = f2(a0, a1);
+              acc2[e & 1] = f2_add(acc2[e & 1], a2);
+              const uint32_t hi = pack_bf16x2(a0, a1);
+              pk[c][e] = hi;
+              float r0, r1;
+              f2_split(f2_sub(a2, f2(bf_lo(hi), bf_hi(hi))), r0, r1);
+              pl[c][e] = pack_bf16x2(r0, r1);
             }
           }
-          rs = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-          if constexpr (TRACK) mx = fmaxf(mxl[0], mxl[1]);
+          float s0, s1, s2, s3;
+          f2_split(acc2[0], s0, s1);
+          f2_split(acc2[1], s2, s3);
+          rs = (s0 + s1) + (s2 + s3);
+          if constexpr (TRACK) mx = mxl;
         };
         if (full) pass(m, std::true_type{}, std::true_type{});
         else pass(m, std::false_type{}, std::true_type{});
