@@ -421,3 +421,29 @@ def test_cascade_bad_prefix_block_id_is_flagged(pkvlib):
                max_query_len=1, shared_prefix_pages=32)
     torch.cuda.synchronize()
     assert pkv.get_last_error() & pkv.STATUS_BAD_BLOCK
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_mixed_length_chunks_beside_decode_rows(pkvlib, seed):
+    """Two dozen chunks of 9 to 200 query tokens over up to 3000 cached keys,
+    every fifth row a decode row: query groups of every length and ragged
+    last tiles in one prefill launch beside split-KV.  Every row against the
+    oracle; three calls on one workspace give the same bits."""
+    rng = np.random.default_rng(950 + seed)
+    B = 24
+    qlens = rng.integers(9, 200, size=B)
+    lens = qlens + rng.integers(0, 3000, size=B)
+    qlens[::5] = 1  # decode rows beside them
+    b = make_batch(lens.tolist(), qlens.tolist(), 32, 8, seed=960 + seed, device="cuda")
+    meta = to_device(b)
+    kc, vc = b.k_cache.clone(), b.v_cache.clone()
+    pkv.write(b.k_new, b.v_new, meta["slot_mapping"], kc, vc)
+    ws = torch.empty(pkv.workspace_size(pkv.make_desc(kc, b.num_q_heads, b.block_tables.shape[1]), b.B, b.T),
+                     dtype=torch.uint8, device="cuda")
+    outs = [pkv.attend(b.q, kc, vc, meta["block_tables"], meta["seq_lens"], meta["query_start_loc"], b.scale,
+                       workspace=ws) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert pkv.get_last_error() == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    k_ref, v_ref = oracle_write(b)
+    compare(outs[0], oracle_attend(b, k_ref, v_ref), what=f"mixed-length chunks {seed}")

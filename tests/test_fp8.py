@@ -367,3 +367,13 @@ def test_attend_fp8_prefill_bad_block_ids_are_flagged(pkvlib):
     expected = O.attend_fp8(bits(b.q), *ref, b.block_tables, b.seq_lens, b.query_start_loc, b.scale,
                             b.num_q_heads, b.num_kv_heads, b.page_size, rows=rows)
     compare(out, expected, rows=rows, what="fp8 rows beside bad block ids")
+
+
+def test_attend_fp8_mixed_length_chunks(pkvlib):
+    """FP8 pages: chunks of 9 to 200 query tokens over up to 3000 cached keys
+    in one prefill launch, ragged last tiles of every length."""
+    rng = np.random.default_rng(970)
+    qlens = rng.integers(9, 200, size=20)
+    lens = qlens + rng.integers(0, 3000, size=20)
+    _run(make_batch(lens.tolist(), qlens.tolist(), 32, 8, seed=971, device="cuda"), 972,
+         what="fp8 mixed-length chunks")
