@@ -1084,20 +1084,6 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
         ka[c] = swz(Kp, 2 * gq + (tq >> 1), 4 * (tq & 1) + c);
         kb[c] = swz(Kp, 2 * (gq + 8) + (tq >> 1), 4 * (tq & 1) + c);
       }
-      // V rows tq, tq+4, tq+8, tq+12: dims 8gq..8gq+7 (chunk gq of the first
-      // unit) and 64+8gq..64+8gq+7 (chunk gq of the second)
-      uint4 vr[4][2];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-#pragma unroll
-        for (int x = 0; x < 4; ++x) vr[x][c] = swz(Vp, 2 * (tq + 4 * x) + c, gq);
-      }
-      __syncwarp();
-      if (it + NS < n_units) {
-        issue(stage);
-        if (it + NS + 1 < n_units) cursor_advance(pc, p, sq, per_row);
-      }
-
       // ---- S^T = K . Q^T ----
       float sacc[4] = {0.f, 0.f, 0.f, 0.f};
       {
@@ -1112,6 +1098,20 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) sacc[e] += sodd[e];
+      }
+      // V rows tq, tq+4, tq+8, tq+12: dims 8gq..8gq+7 (chunk gq of the first
+      // unit) and 64+8gq..64+8gq+7 (chunk gq of the second).  Read after the
+      // S products, so that K's and V's fragments are never live together.
+      uint4 vr[4][2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int x = 0; x < 4; ++x) vr[x][c] = swz(Vp, 2 * (tq + 4 * x) + c, gq);
+      }
+      __syncwarp();
+      if (it + NS < n_units) {
+        issue(stage);
+        if (it + NS + 1 < n_units) cursor_advance(pc, p, sq, per_row);
       }
       const bool t0 = gq < nvalid, t1 = gq + 8 < nvalid;
       const bool h0 = 2 * tq < 2 * GH, h1r = 2 * tq + 1 < 2 * GH;
