@@ -248,7 +248,8 @@ def test_long_chunks_run_on_the_tensor_core_kernel(pkvlib):
 
 
 @pytest.mark.parametrize("hq,hkv,L,n", [(32, 8, 1100, 130), (16, 2, 257, 257), (8, 8, 640, 300),
-                                        (32, 2, 129, 33), (64, 4, 3000, 17), (32, 8, 2000, 100)])
+                                        (32, 2, 129, 33), (64, 4, 3000, 17), (32, 8, 2000, 100),
+                                        (16, 8, 700, 200)])
 def test_prefill_chunks_all_rows(pkvlib, hq, hkv, L, n):
     """Chunks spanning several 128-key tiles with ragged ends, every row."""
     b = make_batch([L, 40], [n, 1], hq, hkv, seed=L + n, device="cuda")
@@ -256,6 +257,17 @@ def test_prefill_chunks_all_rows(pkvlib, hq, hkv, L, n):
     assert counts["prefill"] == 1
     k_ref, v_ref = oracle_write(b)
     compare(out, oracle_attend(b, k_ref, v_ref), what=f"prefill {hq}/{hkv} L={L} n={n}")
+
+
+def test_prefill_chunk_over_a_long_context(pkvlib):
+    """A 40-token chunk at the end of a 16,384-token sequence: its query
+    group runs 128 K/V tiles, so the tile buffers and their barriers wrap
+    their phases many times.  Every row against the oracle."""
+    b = make_batch([16384, 300], [40, 1], 32, 8, seed=990, device="cuda")
+    counts, out, _, _ = _kernel_launches(b, 40)
+    assert counts["prefill"] == 1
+    k_ref, v_ref = oracle_write(b)
+    compare(out, oracle_attend(b, k_ref, v_ref), what="prefill over 16k keys")
 
 
 def test_prefill_chunks_of_several_sequences(pkvlib):

@@ -167,7 +167,8 @@ def test_attend_fp8_stale_rows_do_not_leak(pkvlib):
 
 
 @pytest.mark.parametrize("hq,hkv,L,n", [(32, 8, 1100, 130), (16, 2, 257, 257), (8, 8, 640, 300),
-                                        (32, 2, 129, 33), (64, 4, 3000, 17), (32, 8, 2000, 100)])
+                                        (32, 2, 129, 33), (64, 4, 3000, 17), (32, 8, 2000, 100),
+                                        (16, 8, 700, 200)])
 def test_attend_fp8_prefill_chunks_all_rows(pkvlib, hq, hkv, L, n):
     """Chunks longer than the split-KV bound run on the tensor-core kernel, the
     pages widened exactly to bf16 in shared memory; every row."""
