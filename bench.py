@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
                     help="page format: bf16, or E4M3 codes with per-row scale bytes")
+    ap.add_argument("--transfer", action="store_true",
+                    help="time page export/import (the workload's pages to and from a device buffer and "
+                         "pinned host memory) instead of the attend step")
     return ap.parse_args()
 
 
@@ -343,6 +346,73 @@ def config_of(b, idx, kv="bf16"):
             "l2": "pool larger than L2; L2 flushed before every timed step, outside its events (256 MiB write, then a 256 MiB read so no dirty lines remain)"}
 
 
+def run_transfer(args, rank, world, local):
+    """Page export/import of every page the workload's block tables name: to
+    a device buffer (HBM to HBM) and to pinned host memory (over the GPU's
+    link to the host), and back.  Payload GB/s per direction; the device
+    copy also against the measured HBM copy peak (read + write)."""
+    import paged_kv_cache_pkv_gb300 as pkv
+    from workloads import workload
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    b = workload(args.workload, device=dev)
+    pages_np = np.unique(np.concatenate([b.block_tables[i, :(int(b.seq_lens[i]) + 15) // 16]
+                                         for i in range(b.B)]))
+    pages = torch.from_numpy(pages_np.astype(np.int32)).to(dev)
+    n = pages.shape[0]
+    kc, vc = b.k_cache, b.v_cache
+    page_bytes = 2 * kc[0].numel() * 2  # K and V of one page, all kv heads
+    payload = n * page_bytes
+    dbuf = torch.empty((n, 2) + tuple(kc.shape[1:]), dtype=torch.bfloat16, device=dev)
+    hbuf = torch.empty((n, 2) + tuple(kc.shape[1:]), dtype=torch.bfloat16, pin_memory=True)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    steps = max(1, min(args.steps, 50))
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            c.record(stream)
+            ts.append((a, c))
+        torch.cuda.synchronize()
+        return float(np.median([a.elapsed_time(c) for a, c in ts])) / 1e3
+
+    res = {}
+    for name, fn in (("export_device", lambda: pkv.export_pages(kc, vc, pages, out=dbuf)),
+                     ("import_device", lambda: pkv.import_pages(dbuf, pages, kc, vc)),
+                     ("export_host", lambda: pkv.export_pages(kc, vc, pages, out=hbuf)),
+                     ("import_host", lambda: pkv.import_pages(hbuf, pages, kc, vc))):
+        sec = timed(fn)
+        res[name] = {"us": sec * 1e6, "payload_gbs": payload / sec / 1e9}
+    # the link's reference: one copy-engine copy of the same bytes, contiguous
+    for name, fn in (("copy_engine_h2d", lambda: dbuf.copy_(hbuf, non_blocking=True)),
+                     ("copy_engine_d2h", lambda: hbuf.copy_(dbuf, non_blocking=True))):
+        sec = timed(fn)
+        res[name] = {"us": sec * 1e6, "payload_gbs": payload / sec / 1e9}
+    for k, ref in (("export_host", "copy_engine_d2h"), ("import_host", "copy_engine_h2d")):
+        res[k]["of_copy_engine"] = res[k]["payload_gbs"] / res[ref]["payload_gbs"]
+    if pkv.get_last_error():
+        raise RuntimeError("device status flags set during the transfer timing")
+    peaks, peak_kind = measured_peaks()
+    for k in ("export_device", "import_device"):
+        res[k]["hbm_frac"] = 2 * res[k]["payload_gbs"] / peaks["hbm_gbs"]
+    if rank == 0:
+        print(json.dumps({"metric": "KV page export/import GB/s (payload per direction)", "impl": "pkv",
+                          "pages": n, "payload_bytes": payload, "data": "synthetic",
+                          "config": {"workload": f"cfg{args.workload}: every page its block tables name"},
+                          "hbm_peak_gbs": peaks["hbm_gbs"], "peak_kind": peak_kind,
+                          "timing": "median of CUDA-event pairs, L2 flushed before each", "results": res}),
+              flush=True)
+
+
 # ---------------------------------------------------------------------------
 # the library
 # ---------------------------------------------------------------------------
@@ -351,6 +421,9 @@ def main():
     rank, world, local = dist_init(args)
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.transfer:
+        run_transfer(args, rank, world, local)
         return
     import paged_kv_cache_pkv_gb300 as pkv
     from workloads import fp8_pools, kv_bytes, workload
