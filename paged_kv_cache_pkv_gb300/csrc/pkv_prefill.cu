@@ -64,6 +64,14 @@ namespace pkv {
 
 constexpr int kPfSoftmaxThreads = 256;  // two threads per query row (64 score columns each)
 constexpr int kPfThreads = kPfSoftmaxThreads + 128;  // + K-load, V-load and two MMA warps
+// FP8 pages: four more warps, a second widening warp for K and one for V
+// (two idle), so each operand's pages are widened by two warps.  The block's
+// 512 threads launch with 128 registers each; the softmax warpgroups raise
+// theirs to 160 and the other two lower theirs to 96 (2 x 128 x 160 +
+// 2 x 128 x 96 = 65536, the launch's total, so the raise never waits on
+// registers that are not there).
+template <bool F8>
+constexpr int kPfThreadsOf = F8 ? kPfThreads + 128 : kPfThreads;
 constexpr int kPfPagesPerTile = kPfKeys / kPage;
 constexpr uint32_t kTmemCols = 512;   // S/P of Q tile 0 [0,128), of tile 1 [128,256), O0 [256,384), O1 [384,512)
 constexpr float kPfTau = 8.0f;
@@ -389,7 +397,7 @@ __device__ __forceinline__ void widen_row_half(const uint8_t* spage, uint32_t sb
 // PREFIX = true: every query row against the shared prefix keys, written as
 // log-sum-exp partial records that the split-KV kernel merges.
 template <bool PREFIX, bool F8>
-__global__ void __launch_bounds__(kPfThreads, 1)
+__global__ void __launch_bounds__(kPfThreadsOf<F8>, 1)
     pkv_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, PrefillParams p) {
@@ -411,8 +419,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint8_t* sV = sm + kOffV;
   // misc region: barriers, TMEM address, tile info, scan sums, row exchange
   constexpr uint32_t kOffM = kMiscOf<F8>;
-  constexpr int kBars = 7 + 6 * kKVBufs + 2;
-  static_assert(kBars * 8 <= 192 && 208 + 4 * (kPfThreads / 32) <= 256 && 256 + 2 * 128 * 4 <= kPfMisc,
+  constexpr int kNT = kPfThreadsOf<F8>;
+  constexpr int kBars = 7 + 6 * kKVBufs + 4;
+  static_assert(kBars * 8 <= 192 && 208 + 4 * (kNT / 32) <= 320 && 320 + 2 * 128 * 4 <= kPfMisc,
                 "prefill misc region layout");
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffM);
   uint64_t* bar_q = bars;                     // both Q tiles landed
@@ -423,12 +432,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t* bar_v = bar_k + kKVBufs;          // [kKVBufs] V tile landed in buffer b
   uint64_t* bar_kfree = bar_v + kKVBufs;          // [kKVBufs][2] the S MMAs of Q tile u reading K buffer b are done
   uint64_t* bar_vfree = bar_kfree + 2 * kKVBufs;  // [kKVBufs][2] the PV MMAs of Q tile u reading V buffer b are done
-  uint64_t* bar_kst = bar_vfree + 2 * kKVBufs;     // FP8: a K tile's codes and scales staged
-  uint64_t* bar_vst = bar_kst + 1;                 // FP8: a V tile's codes and scales staged
+  uint64_t* bar_kst = bar_vfree + 2 * kKVBufs;     // FP8: [2 slices] a K tile's codes and scales staged
+  uint64_t* bar_vst = bar_kst + 2;                 // FP8: [2 slices] a V tile's codes and scales staged
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffM + 192);  // after 24 barrier slots
   int* s_info = reinterpret_cast<int*>(sm + kOffM + 200);  // b, t0
   int* s_scan = reinterpret_cast<int*>(sK);  // plan scratch (before any K tile lands)
-  int* s_wsum = reinterpret_cast<int*>(sm + kOffM + 208);  // [warps] scan sums
+  int* s_wsum = reinterpret_cast<int*>(sm + kOffM + 208);  // [warps] scan sums (up to 16 warps)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = blockIdx.x;  // kv head; blockIdx.y = query group (real groups dispatch first)
@@ -453,7 +462,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     b = c;  // chunk index (record slot)
     if (nkv <= 0) return;
   } else {
-    const int per = (p.B + kPfThreads - 1) / kPfThreads;
+    const int per = (p.B + kNT - 1) / kNT;
     const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
     int local = 0;
     for (int bb = b0; bb < b1; ++bb) {
@@ -475,7 +484,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __syncthreads();
     int base = 0, total = 0;
 #pragma unroll
-    for (int x = 0; x < kPfThreads / 32; ++x) {
+    for (int x = 0; x < kNT / 32; ++x) {
       if (x < warp) base += s_wsum[x];
       total += s_wsum[x];
     }
@@ -525,9 +534,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   // ---- barriers and TMEM -----------------------------------------------------
   if (tid == 0) {
     // each barrier initialised once: P ready takes the 256 softmax arrivals,
+    // a K or V tile on FP8 pages the arrivals of its two widening warps,
     // every other barrier one arrival (a TMA transaction or a commit)
-    for (int i = 0; i < kBars; ++i)
-      mbar_init(bars + i, (bars + i == bar_p || bars + i == bar_p + 1) ? kPfSoftmaxThreads : 1);
+    for (int i = 0; i < kBars; ++i) {
+      const bool kv = bars + i >= bar_k && bars + i < bar_k + 2 * kKVBufs;
+      mbar_init(bars + i, (bars + i == bar_p || bars + i == bar_p + 1) ? kPfSoftmaxThreads : (F8 && kv) ? 2 : 1);
+    }
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -548,7 +560,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   auto tmem_o = [&](int u) { return tmem + 256 + uint32_t(u) * 128; };
   const uint32_t idesc_s = idesc_bf16(128, 128, false);
   const uint32_t idesc_o = idesc_bf16(128, 128, true);
-  const int role = warp - kPfSoftmaxThreads / 32;  // 0: K loads, 1: V loads, 2 + u: MMA of Q tile u; < 0 softmax
+  // 0: K loads, 1: V loads, 2 + u: MMA of Q tile u; < 0 softmax; FP8 pages:
+  // 4 and 5 the second K and V widening warps, 6 and 7 idle
+  const int role = warp - kPfSoftmaxThreads / 32;
   // With FP8 pages the loader warps widen every tile and set the pace; the
   // softmax and MMA warps, which share their sub-partitions, sleep between
   // barrier tests instead of spinning.
@@ -570,17 +584,27 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   };
 
-  if (role == 0 || role == 1) {
+  if (role >= 0) {
+  // FP8 pages: the loader, MMA and idle warps (two whole warpgroups) give up
+  // registers here for the softmax warpgroups, which take them below
+  if constexpr (F8) asm volatile("setmaxnreg.dec.sync.aligned.u32 96;");
+  if (role == 0 || role == 1 || (F8 && (role == 4 || role == 5))) {
     // ===== K or V producer (lane 0 issues; the warp fetches block ids) =====
+    // FP8 pages: slice 0 (roles 0, 1) widens pages 0-3 of each tile, slice 1
+    // (roles 4, 5) pages 4-7, each with its own staging barrier; both arrive
+    // on the tile's barrier.
+    const int op = role & 1, slice = role >> 2;
+    const int j0 = F8 ? slice * (kPfPagesPerTile / 2) : 0;
+    const int j1 = F8 ? j0 + kPfPagesPerTile / 2 : kPfPagesPerTile;
     // Buffer kt % kKVBufs is free once the MMAs that read tile kt - kKVBufs
     // are done (the S of every Q tile for K, their PV for V; each buffer has
     // its own barrier, so no wait targets a phase more than one behind).
     // Block ids come in groups of four tiles, one page per lane, read a group
     // ahead: a tile's copies never wait on a block-table read.
-    const CUtensorMap* map = role == 0 ? &tm_k : &tm_v;
-    uint8_t* base0 = role == 0 ? sK : sV;
-    uint64_t* bar_load = role == 0 ? bar_k : bar_v;
-    uint64_t* bar_free = role == 0 ? bar_kfree : bar_vfree;
+    const CUtensorMap* map = op == 0 ? &tm_k : &tm_v;
+    uint8_t* base0 = op == 0 ? sK : sV;
+    uint64_t* bar_load = op == 0 ? bar_k : bar_v;
+    uint64_t* bar_free = op == 0 ? bar_kfree : bar_vfree;
     if (role == 0 && lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
       mbar_arrive_expect_tx(bar_q, uint32_t(nt) * 2 * kHalfTile);
@@ -610,15 +634,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     bool ok = true;
     // FP8 pages: the tile's codes and scales go to a staging area first (lane
     // 0 issues), and the warp widens them into the bf16 tile buffer.
-    uint8_t* stage = sm + (role == 0 ? kOffStageK : kOffStageV);
-    uint8_t* ssc = sm + (role == 0 ? kOffScK : kOffScV);
-    const uint8_t* scl = role == 0 ? p.k_scale : p.v_scale;
-    uint64_t* bar_st = role == 0 ? bar_kst : bar_vst;
+    uint8_t* stage = sm + (op == 0 ? kOffStageK : kOffStageV);
+    uint8_t* ssc = sm + (op == 0 ? kOffScK : kOffScV);
+    const uint8_t* scl = op == 0 ? p.k_scale : p.v_scale;
+    uint64_t* bar_st = (op == 0 ? bar_kst : bar_vst) + slice;  // this slice's pages j0..j1-1
     int st_pending = -1;  // tile whose staging copies are out and not yet waited for
     auto arm_stage = [&](const int (&bids)[kPfPagesPerTile]) {
       int valid = 0;
 #pragma unroll
-      for (int j = 0; j < kPfPagesPerTile; ++j) valid += bids[j] >= 0;
+      for (int j = 0; j < kPfPagesPerTile; ++j) valid += j >= j0 && j < j1 && bids[j] >= 0;
       mbar_arrive_expect_tx(bar_st, uint32_t(valid) * (kStagePage + kScaleBytes));
     };
     auto stage_page = [&](int j, int bid) {
@@ -631,7 +655,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int j = 0; j < kPfPagesPerTile; ++j) ids0[j] = __shfl_sync(0xffffffffu, cur_g, j);
       if (lane == 0) {
         arm_stage(ids0);
-        for (int j = 0; j < kPfPagesPerTile; ++j)
+        for (int j = j0; j < j1; ++j)
           if (ids0[j] >= 0) stage_page(j, ids0[j]);
       }
       st_pending = 0;
@@ -670,7 +694,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         st_pending = -1;
         if (kn < nkv) {
           if (lane == 0) {
-            const int valid = __popc((nvalid_mask >> nxt_lane0) & 0xFFu);
+            const int valid = __popc((nvalid_mask >> (nxt_lane0 + j0)) & ((1u << (j1 - j0)) - 1u));
             mbar_arrive_expect_tx(bar_st, uint32_t(valid) * (kStagePage + kScaleBytes));
           }
           st_pending = kn;
@@ -678,7 +702,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         uint8_t* dst = base0 + kb * 2 * kHalfTile;
         const int r = lane >> 1, h = lane & 1;
 #pragma unroll 1
-        for (int j = 0; j < kPfPagesPerTile; ++j) {
+        for (int j = j0; j < j1; ++j) {
           const int idj = __shfl_sync(0xffffffffu, cur_g, cur_lane0 + j);
           const int nidj = __shfl_sync(0xffffffffu, src_g, nxt_lane0 + j);
           if (idj >= 0)
@@ -701,7 +725,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (!ok) flag_status(p.status, PKV_STATUS_TIMEOUT);
     }
     __syncwarp();
-  } else if (role >= 2) {
+  } else if (role == 2 || role == 3) {
     // ===== MMA issuers: one lane per Q tile =====
     // Per K/V tile kt: PV(u, kt) as soon as P(u, kt) is written, then S(u,
     // kt+1) into the same TMEM columns (issued after the PV that reads P
@@ -759,7 +783,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (npv > 0) mbar_wait(bar_o + u, (npv - 1) & 1, ok ? kLandLimitNs : kDrainLimitNs);
     }
     __syncwarp();
+  }
   } else {
+    if constexpr (F8) asm volatile("setmaxnreg.inc.sync.aligned.u32 160;");
     // ===== softmax warps: Q tiles 0 and 1 in turn =====
     const int r = tid & 127;  // query row == TMEM lane
     const int ch = tid >> 7;  // which 64 of the 128 score columns
@@ -775,7 +801,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     // running max (same in both threads of a row) and half row sum, per tile
     float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
-    float* s_red = reinterpret_cast<float*>(sm + kOffM + 256);  // [2][128] exchange
+    float* s_red = reinterpret_cast<float*>(sm + kOffM + 320);  // [2][128] exchange
     // ok: this thread's waits all succeeded.  stop: some softmax thread's
     // failed, decided at the same barrier by all 256 of them, so they leave
     // the loop together (the loop holds named barriers).
@@ -1121,7 +1147,7 @@ int launch_prefill(const LaunchCtx& ctx, const AttendArgs& a, int split_max_q, i
   pp.epoch = epoch;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.desc.num_kv_heads, prefill_groups(a.desc, a.num_seqs, a.num_tokens, max_tiles));
-  cfg.blockDim = dim3(kPfThreads);
+  cfg.blockDim = dim3(a.fp8 ? kPfThreadsOf<true> : kPfThreadsOf<false>);
   cfg.dynamicSmemBytes = a.fp8 ? kPfSmemOf<true> : kPfSmemOf<false>;
   cfg.stream = ctx.stream;
   // behind the split-KV kernel: start once its CTAs let it (their pool reads
@@ -1171,10 +1197,10 @@ int launch_prefix(const LaunchCtx& ctx, const AttendArgs& a, float* records, int
   const int qgroups = (a.num_tokens + pp.TM - 1) / pp.TM;
   TraceScope ts(ctx.stream, PKV_K_PREFILL);
   if (a.fp8)
-    pkv_prefill_kernel<true, true><<<dim3(a.desc.num_kv_heads, qgroups * chunks), kPfThreads,
+    pkv_prefill_kernel<true, true><<<dim3(a.desc.num_kv_heads, qgroups * chunks), kPfThreadsOf<true>,
                                      kPfSmemOf<true>, ctx.stream>>>(tq, tk, tv, pp);
   else
-    pkv_prefill_kernel<true, false><<<dim3(a.desc.num_kv_heads, qgroups * chunks), kPfThreads,
+    pkv_prefill_kernel<true, false><<<dim3(a.desc.num_kv_heads, qgroups * chunks), kPfThreadsOf<false>,
                                       kPfSmemOf<false>, ctx.stream>>>(tq, tk, tv, pp);
   return ts.done();
 }
