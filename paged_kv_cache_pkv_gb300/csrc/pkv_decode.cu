@@ -1237,16 +1237,16 @@ int decode_ctas_per_sm(int variant, bool fp8) {
 // pass runs behind it; 0 puts the pass first instead.  Measured on the
 // 96-row mixed step (two 512-token chunks; 2,880 steps against 188,544
 // units): bf16 1900 / 2300 / 2600 / 3000 -> 298 / 270 / 271 / 271 us.  FP8
-// pages (the pass widens codes with two warps per operand, about 4.7 us a
+// pages (the pass widens codes with three warps per operand, about 4 us a
 // step, and split-KV is bound by issue, so the SMs are split in
-// proportion): 5000 / 6500 / 8000 / 9000 / 10000 -> 297 / 287 / 296 / 310 /
-// 324 us (pass first: 340 us).
+// proportion): 4000 / 5000 / 6500 -> 275 / 255 / 275 us (pass first: 340
+// us).
 static int prefill_step_units(bool fp8) {
   static int v[2] = {-1, -1};
   int& x = v[fp8 ? 1 : 0];
   if (x < 0) {
     const char* e = getenv(fp8 ? "PKV_PREFILL_STEP_UNITS_FP8" : "PKV_PREFILL_STEP_UNITS");
-    x = e ? atoi(e) : (fp8 ? 6500 : 2400);
+    x = e ? atoi(e) : (fp8 ? 5000 : 2400);
   }
   return x;
 }

@@ -64,8 +64,9 @@ namespace pkv {
 
 constexpr int kPfSoftmaxThreads = 256;  // two threads per query row (64 score columns each)
 constexpr int kPfThreads = kPfSoftmaxThreads + 128;  // + K-load, V-load and two MMA warps
-// FP8 pages: four more warps, a second widening warp for K and one for V
-// (two idle), so each operand's pages are widened by two warps.  The block's
+// FP8 pages: four more warps, a second and a third widening warp for K and
+// for V, so each operand's eight pages a tile are widened by three warps
+// (pages 0-2, 3-5, 6-7).  The block's
 // 512 threads launch with 128 registers each; the softmax warpgroups raise
 // theirs to 160 and the other two lower theirs to 96 (2 x 128 x 160 +
 // 2 x 128 x 96 = 65536, the launch's total, so the raise never waits on
@@ -420,8 +421,8 @@ __global__ void __launch_bounds__(kPfThreadsOf<F8>, 1)
   // misc region: barriers, TMEM address, tile info, scan sums, row exchange
   constexpr uint32_t kOffM = kMiscOf<F8>;
   constexpr int kNT = kPfThreadsOf<F8>;
-  constexpr int kBars = 7 + 6 * kKVBufs + 4;
-  static_assert(kBars * 8 <= 192 && 208 + 4 * (kNT / 32) <= 320 && 320 + 2 * 128 * 4 <= kPfMisc,
+  constexpr int kBars = 7 + 6 * kKVBufs + 6;
+  static_assert(kBars * 8 <= 256 && 272 + 4 * (kNT / 32) <= 384 && 384 + 2 * 128 * 4 <= kPfMisc,
                 "prefill misc region layout");
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffM);
   uint64_t* bar_q = bars;                     // both Q tiles landed
@@ -432,12 +433,12 @@ __global__ void __launch_bounds__(kPfThreadsOf<F8>, 1)
   uint64_t* bar_v = bar_k + kKVBufs;          // [kKVBufs] V tile landed in buffer b
   uint64_t* bar_kfree = bar_v + kKVBufs;          // [kKVBufs][2] the S MMAs of Q tile u reading K buffer b are done
   uint64_t* bar_vfree = bar_kfree + 2 * kKVBufs;  // [kKVBufs][2] the PV MMAs of Q tile u reading V buffer b are done
-  uint64_t* bar_kst = bar_vfree + 2 * kKVBufs;     // FP8: [2 slices] a K tile's codes and scales staged
-  uint64_t* bar_vst = bar_kst + 2;                 // FP8: [2 slices] a V tile's codes and scales staged
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffM + 192);  // after 24 barrier slots
-  int* s_info = reinterpret_cast<int*>(sm + kOffM + 200);  // b, t0
+  uint64_t* bar_kst = bar_vfree + 2 * kKVBufs;     // FP8: [3 slices] a K tile's codes and scales staged
+  uint64_t* bar_vst = bar_kst + 3;                 // FP8: [3 slices] a V tile's codes and scales staged
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffM + 256);  // after 32 barrier slots
+  int* s_info = reinterpret_cast<int*>(sm + kOffM + 264);  // b, t0
   int* s_scan = reinterpret_cast<int*>(sK);  // plan scratch (before any K tile lands)
-  int* s_wsum = reinterpret_cast<int*>(sm + kOffM + 208);  // [warps] scan sums (up to 16 warps)
+  int* s_wsum = reinterpret_cast<int*>(sm + kOffM + 272);  // [warps] scan sums (up to 16 warps)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = blockIdx.x;  // kv head; blockIdx.y = query group (real groups dispatch first)
@@ -534,11 +535,11 @@ __global__ void __launch_bounds__(kPfThreadsOf<F8>, 1)
   // ---- barriers and TMEM -----------------------------------------------------
   if (tid == 0) {
     // each barrier initialised once: P ready takes the 256 softmax arrivals,
-    // a K or V tile on FP8 pages the arrivals of its two widening warps,
+    // a K or V tile on FP8 pages the arrivals of its three widening warps,
     // every other barrier one arrival (a TMA transaction or a commit)
     for (int i = 0; i < kBars; ++i) {
       const bool kv = bars + i >= bar_k && bars + i < bar_k + 2 * kKVBufs;
-      mbar_init(bars + i, (bars + i == bar_p || bars + i == bar_p + 1) ? kPfSoftmaxThreads : (F8 && kv) ? 2 : 1);
+      mbar_init(bars + i, (bars + i == bar_p || bars + i == bar_p + 1) ? kPfSoftmaxThreads : (F8 && kv) ? 3 : 1);
     }
     fence_mbar_init();
   }
@@ -561,7 +562,7 @@ __global__ void __launch_bounds__(kPfThreadsOf<F8>, 1)
   const uint32_t idesc_s = idesc_bf16(128, 128, false);
   const uint32_t idesc_o = idesc_bf16(128, 128, true);
   // 0: K loads, 1: V loads, 2 + u: MMA of Q tile u; < 0 softmax; FP8 pages:
-  // 4 and 5 the second K and V widening warps, 6 and 7 idle
+  // 4 and 5 the second K and V widening warps, 6 and 7 the third
   const int role = warp - kPfSoftmaxThreads / 32;
   // With FP8 pages the loader warps widen every tile and set the pace; the
   // softmax and MMA warps, which share their sub-partitions, sleep between
@@ -585,17 +586,17 @@ __global__ void __launch_bounds__(kPfThreadsOf<F8>, 1)
   };
 
   if (role >= 0) {
-  // FP8 pages: the loader, MMA and idle warps (two whole warpgroups) give up
+  // FP8 pages: the loader and MMA warps (two whole warpgroups) give up
   // registers here for the softmax warpgroups, which take them below
   if constexpr (F8) asm volatile("setmaxnreg.dec.sync.aligned.u32 96;");
-  if (role == 0 || role == 1 || (F8 && (role == 4 || role == 5))) {
+  if (role == 0 || role == 1 || (F8 && role >= 4)) {
     // ===== K or V producer (lane 0 issues; the warp fetches block ids) =====
-    // FP8 pages: slice 0 (roles 0, 1) widens pages 0-3 of each tile, slice 1
-    // (roles 4, 5) pages 4-7, each with its own staging barrier; both arrive
-    // on the tile's barrier.
-    const int op = role & 1, slice = role >> 2;
-    const int j0 = F8 ? slice * (kPfPagesPerTile / 2) : 0;
-    const int j1 = F8 ? j0 + kPfPagesPerTile / 2 : kPfPagesPerTile;
+    // FP8 pages: slice 0 (roles 0, 1) widens pages 0-2 of each tile, slice 1
+    // (roles 4, 5) pages 3-5, slice 2 (roles 6, 7) pages 6-7, each with its
+    // own staging barrier; all three arrive on the tile's barrier.
+    const int op = role & 1, slice = role < 2 ? 0 : (role - 2) >> 1;
+    const int j0 = F8 ? (slice == 0 ? 0 : slice == 1 ? 3 : 6) : 0;
+    const int j1 = F8 ? (slice == 0 ? 3 : slice == 1 ? 6 : kPfPagesPerTile) : kPfPagesPerTile;
     // Buffer kt % kKVBufs is free once the MMAs that read tile kt - kKVBufs
     // are done (the S of every Q tile for K, their PV for V; each buffer has
     // its own barrier, so no wait targets a phase more than one behind).
@@ -801,7 +802,7 @@ __global__ void __launch_bounds__(kPfThreadsOf<F8>, 1)
     }
     // running max (same in both threads of a row) and half row sum, per tile
     float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
-    float* s_red = reinterpret_cast<float*>(sm + kOffM + 320);  // [2][128] exchange
+    float* s_red = reinterpret_cast<float*>(sm + kOffM + 384);  // [2][128] exchange
     // ok: this thread's waits all succeeded.  stop: some softmax thread's
     // failed, decided at the same barrier by all 256 of them, so they leave
     // the loop together (the loop holds named barriers).
