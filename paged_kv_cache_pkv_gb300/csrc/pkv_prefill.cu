@@ -1074,6 +1074,18 @@ static int ensure_prefill_attr(int device) {
       cudaGetLastError();
       return PKV_ERR_LAUNCH;
     }
+    if constexpr (F8) {
+      // The warpgroups' register split (softmax up to 160, the rest down to
+      // 96) needs the block launched with at least 128 registers a thread:
+      // with fewer, the softmax warpgroups' raise would wait for registers
+      // that never come.  Refuse to launch a build where that is not so.
+      cudaFuncAttributes fa{};
+      if (cudaFuncGetAttributes(&fa, pkv_prefill_kernel<PREFIX, F8>) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_LAUNCH;
+      }
+      if (fa.numRegs * kPfThreadsOf<F8> < 2 * 128 * 160 + 2 * 128 * 96) return PKV_ERR_LAUNCH;
+    }
     done[device] = true;
   }
   return PKV_OK;
