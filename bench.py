@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
                     help="page format: bf16, or E4M3 codes with per-row scale bytes")
+    ap.add_argument("--hot-l2", action="store_true",
+                    help="no L2 flush between the timed steps (hot-L2 figures, reported separately; "
+                         "the default flushes)")
     ap.add_argument("--transfer", action="store_true",
                     help="time page export/import (the workload's pages to and from a device buffer and "
                          "pinned host memory) instead of the attend step")
@@ -335,7 +338,7 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def config_of(b, idx, kv="bf16"):
+def config_of(b, idx, kv="bf16", hot_l2=False):
     from workloads import WORKLOADS
     return {"workload": f"cfg{idx}: {WORKLOADS[idx]}" + (", FP8 (E4M3) pages" if kv == "fp8" else ""),
             "kv_pages": "bf16" if kv == "bf16" else "E4M3 codes + one power-of-two scale byte per row",
@@ -343,7 +346,9 @@ def config_of(b, idx, kv="bf16"):
             "num_q_heads": b.num_q_heads, "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim,
             "page_size": b.page_size, "pool_pages": b.num_blocks,
             "context_tokens": int(b.seq_lens.astype(np.int64).sum()),
-            "l2": "pool larger than L2; L2 flushed before every timed step, outside its events (256 MiB write, then a 256 MiB read so no dirty lines remain)"}
+            "l2": ("hot: no flush between timed steps (what the previous step left in L2 may be reused)" if hot_l2 else
+                   "pool larger than L2; L2 flushed before every timed step, outside its events (256 MiB write, "
+                   "then a 256 MiB read so no dirty lines remain)")}
 
 
 def run_transfer(args, rank, world, local):
@@ -452,6 +457,8 @@ def main():
     evict = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
 
     def flush_l2():
+        if args.hot_l2:
+            return
         flush.zero_()
         evict.sum()
 
@@ -634,7 +641,7 @@ def main():
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
-            "data": "synthetic", "config": config_of(b, args.workload, args.kv),
+            "data": "synthetic", "config": config_of(b, args.workload, args.kv, args.hot_l2),
             "hbm": {"unique_kv_bytes": uniq, "logical_kv_bytes": kv_bytes(b, unique=False, fp8=fp8),
                     "step_gbs": alg_bytes / (total_s / args.steps / world) / 1e9,
                     "step_frac_of_8tbs": alg_bytes / (total_s / args.steps / world) / 1e9 / NOMINAL_HBM_GBS,
