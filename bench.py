@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--hot-l2", action="store_true",
                     help="no L2 flush between the timed steps (hot-L2 figures, reported separately; "
                          "the default flushes)")
+    ap.add_argument("--prefill-alone", action="store_true",
+                    help="time the tensor-core prefill pass alone on the mixed step's two 512-token chunks "
+                         "(no decode rows) and report it against the bf16 tensor peak")
     ap.add_argument("--transfer", action="store_true",
                     help="time page export/import (the workload's pages to and from a device buffer and "
                          "pinned host memory) instead of the attend step")
@@ -418,6 +421,86 @@ def run_transfer(args, rank, world, local):
               flush=True)
 
 
+def prefill_pairs(seq_lens, q_lens):
+    """Visible (query, key) pairs of chunks of q_lens new tokens ending
+    sequences of seq_lens tokens (bottom-right causal: new token j of a chunk
+    of n sees L - n + j + 1 keys)."""
+    return sum(n * (L - n) + n * (n + 1) // 2 for L, n in zip(seq_lens, q_lens))
+
+
+def run_prefill_alone(args, rank, world, local):
+    """The tensor-core prefill pass alone: the mixed step's two chunks (512
+    new tokens over 1536 and 3584 cached, 32 q / 8 kv heads) without its
+    decode rows, so the pass has the whole GPU.  FLOPs are the causal
+    attention's, 4 x head_dim per visible (query, key) pair and query head
+    (QK^T and PV, a multiply and an add each); the remainder term of P is
+    not counted.  The kernel time is the mean of CUDA-event pairs around the
+    launches, L2 flushed before each (outside its events)."""
+    import paged_kv_cache_pkv_gb300 as pkv
+    from workloads import fp8_pools, make_batch
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lens, qlens = [1536 + 512, 3584 + 512], [512, 512]
+    b = make_batch(lens, qlens, 32, 8, 1005, device=dev)
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).to(dev)
+    bt, sl, qsl = t(b.block_tables, np.int32), t(b.seq_lens, np.int32), t(b.query_start_loc, np.int32)
+    out = torch.empty_like(b.q)
+    fp8 = args.kv == "fp8"
+    if fp8:
+        kc, vc, ks, vs = fp8_pools(b, 1006)
+        run = lambda: pkv.attend_fp8(b.q, kc, vc, ks, vs, bt, sl, qsl, b.scale, out=out, max_query_len=512)
+    else:
+        run = lambda: pkv.attend(b.q, b.k_cache, b.v_cache, bt, sl, qsl, b.scale, out=out, max_query_len=512)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    evict = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        flush.zero_()
+        evict.sum()
+
+    steps = max(1, min(args.steps, 500))
+    for _ in range(max(args.warmup, 3)):
+        flush_l2()
+        run()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev)
+    clocks.start()
+    launches0 = pkv.launch_count()
+    trace = pkv.Trace(capacity=steps * 4 + 16)
+    with trace:
+        for _ in range(steps):
+            flush_l2()
+            run()
+    torch.cuda.synchronize()
+    launches = pkv.launch_count() - launches0
+    clk = clocks.stop()
+    if pkv.get_last_error():
+        raise RuntimeError("device status flags set during the prefill timing")
+    ms, n = trace.read("prefill")
+    trace.close()
+    if n != steps:
+        raise RuntimeError(f"expected one prefill launch per call, traced {n} for {steps}")
+    avg_s = ms / n / 1e3
+    flop = prefill_pairs(lens, qlens) * b.num_q_heads * 4 * b.head_dim
+    achieved = flop / avg_s / 1e12
+    peaks, peak_kind = measured_peaks()
+    if rank == 0:
+        print(json.dumps({
+            "metric": "tensor-core prefill pass alone: causal attention TFLOP/s, 1xGB300", "impl": "pkv",
+            "value": achieved, "unit": "TFLOP/s", "n_gpus": 1, "steps": steps, "warmup": max(args.warmup, 3),
+            "higher_is_better": True, "dtype": "e4m3 pages, bf16 MMA" if fp8 else "bf16", "data": "synthetic",
+            "config": {"workload": "the mixed step's prefill chunks alone: 2 x 512 new tokens over 1536 and "
+                                   "3584 cached, 32 q / 8 kv heads, head_dim 128"
+                                   + (", FP8 (E4M3) pages" if fp8 else ""),
+                       "l2": "flushed before every launch, outside its events"},
+            "roofline": {"bound": "tensor", "kernel": "pkv_prefill_kernel", "achieved": achieved,
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                         "peak_kind": peak_kind + " (bf16 dense, burst: the kernel timed alone)",
+                         "flop_per_launch": flop, "avg_launch_us": avg_s * 1e6, "traffic": None},
+            "gpu_launches": launches, "clocks": clk}), flush=True)
+
+
 # ---------------------------------------------------------------------------
 # the library
 # ---------------------------------------------------------------------------
@@ -429,6 +512,9 @@ def main():
         return
     if args.transfer:
         run_transfer(args, rank, world, local)
+        return
+    if args.prefill_alone:
+        run_prefill_alone(args, rank, world, local)
         return
     import paged_kv_cache_pkv_gb300 as pkv
     from workloads import fp8_pools, kv_bytes, workload

@@ -39,7 +39,8 @@
 //  * Warp roles: warps 0-7 run the softmax of the two Q tiles in turn; warp 8
 //    loads K tiles, warp 9 loads V tiles (each refills a buffer as soon as
 //    the MMAs that read it are done, with the next tiles' block ids
-//    prefetched), warps 10 and 11 issue the tcgen05.mma of Q tile 0 and 1.
+//    prefetched), warps 10 and 11 issue the tcgen05.mma of Q tile 0 and 1
+//    (each whole warp runs its loop; one elected lane issues).
 //    Pipeline per K/V tile i: PV(0, i) and S(0, i+1) run under the softmax of
 //    Q tile 1, PV(1, i) and S(1, i+1) under the softmax of Q tile 0 for tile
 //    i+1 (the S MMA that overwrites P is issued after the PV that reads it).  Hand-offs are
@@ -159,12 +160,20 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
          (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
+// The MMA helpers are warp-collective: every lane of a converged warp runs
+// them with the same operands and elect.sync picks the one lane that issues.
+// Issued this way (the warp's loop uniform, the instruction predicated)
+// rather than from one lane in a branch of its own, an MMA beside warps of
+// FMA chains on the same sub-partition went from about 600 to about 190
+// cycles, and beside a softmax-like mix from 70-76 to 64-66 (the tensor
+// pipe's rate), in a one-SM probe.
 __device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
                                      uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
@@ -172,15 +181,19 @@ __device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, ui
 __device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
                                         uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
       "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
+// Warp-collective too: the elected lane commits its MMAs to the barrier.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+      "{\n\t.reg .pred e;\n\t.reg .b32 l;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
           smem_u32(bar))
       : "memory");
 }
@@ -727,13 +740,18 @@ __global__ void __launch_bounds__(kPfThreadsOf<F8>, 1)
     }
     __syncwarp();
   } else if (role == 2 || role == 3) {
-    // ===== MMA issuers: one lane per Q tile =====
+    // ===== MMA issuers: one warp per Q tile =====
     // Per K/V tile kt: PV(u, kt) as soon as P(u, kt) is written, then S(u,
     // kt+1) into the same TMEM columns (issued after the PV that reads P
     // there).  The two Q tiles have their own issuing warps, so one tile's
-    // hand-offs never hold up the other's MMAs.
+    // hand-offs never hold up the other's MMAs.  The whole warp runs the
+    // loop and waits; one elected lane issues each MMA and commit.
     const int u = role - 2;
-    if (lane == 0 && u < nt) {
+    // every lane waits; the warp goes on only if all of them saw the phase
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, wait_idle(bar, parity));
+    };
+    if (u < nt) {
       auto issue_s = [&](int kt) {
         const int kb = kt % kKVBufs;
         tc_fence_after();
@@ -748,7 +766,7 @@ __global__ void __launch_bounds__(kPfThreadsOf<F8>, 1)
         umma_commit(bar_kfree + kb * 2 + u);
       };
       int ns = 0, npv = 0;  // S and PV groups issued (for the drain on failure)
-      bool ok = wait_idle(bar_q, 0) && wait_idle(bar_k, 0);
+      bool ok = wait_all(bar_q, 0) && wait_all(bar_k, 0);
       if (ok) {
         issue_s(0);
         ++ns;
@@ -756,7 +774,7 @@ __global__ void __launch_bounds__(kPfThreadsOf<F8>, 1)
       for (int it = 0; ok && it < nkv; ++it) {
         const int vb = it % kKVBufs;
         // P(u, it) written by the softmax; V(it) landed
-        if (!(ok = wait_idle(bar_p + u, it & 1) && wait_idle(bar_v + vb, (it / kKVBufs) & 1))) break;
+        if (!(ok = wait_all(bar_p + u, it & 1) && wait_all(bar_v + vb, (it / kKVBufs) & 1))) break;
         tc_fence_after();
         // 16 keys = 8 packed TMEM columns of P; the remainder term of the
         // same keys sits 32 columns on
@@ -771,15 +789,17 @@ __global__ void __launch_bounds__(kPfThreadsOf<F8>, 1)
         umma_commit(bar_vfree + vb * 2 + u);
         ++npv;
         if (it + 1 < nkv) {
-          if (!(ok = wait_idle(bar_k + (it + 1) % kKVBufs, ((it + 1) / kKVBufs) & 1))) break;
+          if (!(ok = wait_all(bar_k + (it + 1) % kKVBufs, ((it + 1) / kKVBufs) & 1))) break;
           issue_s(it + 1);
           ++ns;
         }
       }
-      if (!ok) flag_status(p.status, PKV_STATUS_TIMEOUT);
-      // this lane's newest commits land before TMEM is released, whatever
-      // the softmax threads' waits saw (each commit covers every earlier MMA
-      // of this lane, and at most one phase of either barrier is pending)
+      if (!ok && lane == 0) flag_status(p.status, PKV_STATUS_TIMEOUT);
+      // this warp's newest commits land before TMEM is released, whatever
+      // the softmax threads' waits saw (the warp stays converged, so
+      // elect.sync picks the same lane for every MMA and commit, and each
+      // commit covers all of that lane's earlier MMAs; at most one phase of
+      // either barrier is pending)
       if (ns > 0) mbar_wait(bar_s + u, (ns - 1) & 1, ok ? kLandLimitNs : kDrainLimitNs);
       if (npv > 0) mbar_wait(bar_o + u, (npv - 1) & 1, ok ? kLandLimitNs : kDrainLimitNs);
     }
