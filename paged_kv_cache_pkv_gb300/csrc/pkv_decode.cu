@@ -196,6 +196,35 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// Warp-collective forms of a page's copy issue: every lane of a converged
+// warp runs them with the same operands and the lane elect.sync picks acts,
+// so the warp never runs the issue code in one lane's branch of its own.
+__device__ __forceinline__ void tma_load_2d_hint_w(void* dst, const CUtensorMap* map, int c0, int c1,
+                                                   uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 l;\n\telect.sync l|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;\n\t}" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_w(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                           uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 l;\n\telect.sync l|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;\n\t}" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_w(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 l;\n\telect.sync l|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr float kTau = 8.0f;  // log2-domain slack before the running max moves
 // Fewest pages a decode warp is given.  Only batches with fewer pages than
@@ -596,23 +625,23 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
     pc.item_start = u_begin - pc.page;
     cursor_bid(pc, p);
   }
+  // warp-collective (every lane holds the same cursor): one elected lane
+  // arms the stage and issues its copies
   auto issue = [&](int stage) {
-    if (lane == 0) {
-      constexpr int PB = kPageBytesOf<F8>;
-      const int g = pc.item / p.nsub;
-      const size_t ph = size_t(pc.bid) * p.Hkv + g;  // (page, kv head)
-      M.desc[stage] = StageDesc{pc.q0 + pc.j, pc.item, pc.item_start, pc.nvis - p.np * kPage};
-      mbar_arrive_expect_tx(&M.bar[stage], 2 * PB + (F8 ? 2 * kScaleBytes : 0));
-      if (kDropFirstCopy && pc.item_start + pc.page == u_begin) return;
-      // one box per page: the pool viewed as [units][128 bytes]; the host
-      // checks that unit indices fit int32
-      const int unit0 = int(ph) * (PB / 128);
-      tma_load_2d_hint(&R.kv[stage][0][0], &tmk, 0, unit0, &M.bar[stage], policy);
-      tma_load_2d_hint(&R.kv[stage][1][0], &tmv, 0, unit0, &M.bar[stage], policy);
-      if constexpr (F8) {
-        bulk_g2s(&M.sc[stage][0], p.k_scale + ph * kScaleBytes, kScaleBytes, &M.bar[stage], policy);
-        bulk_g2s(&M.sc[stage][1], p.v_scale + ph * kScaleBytes, kScaleBytes, &M.bar[stage], policy);
-      }
+    constexpr int PB = kPageBytesOf<F8>;
+    const int g = pc.item / p.nsub;
+    const size_t ph = size_t(pc.bid) * p.Hkv + g;  // (page, kv head)
+    if (lane == 0) M.desc[stage] = StageDesc{pc.q0 + pc.j, pc.item, pc.item_start, pc.nvis - p.np * kPage};
+    mbar_arrive_expect_tx_w(&M.bar[stage], 2 * PB + (F8 ? 2 * kScaleBytes : 0));
+    if (kDropFirstCopy && pc.item_start + pc.page == u_begin) return;
+    // one box per page: the pool viewed as [units][128 bytes]; the host
+    // checks that unit indices fit int32
+    const int unit0 = int(ph) * (PB / 128);
+    tma_load_2d_hint_w(&R.kv[stage][0][0], &tmk, 0, unit0, &M.bar[stage], policy);
+    tma_load_2d_hint_w(&R.kv[stage][1][0], &tmv, 0, unit0, &M.bar[stage], policy);
+    if constexpr (F8) {
+      bulk_g2s_w(&M.sc[stage][0], p.k_scale + ph * kScaleBytes, kScaleBytes, &M.bar[stage], policy);
+      bulk_g2s_w(&M.sc[stage][1], p.v_scale + ph * kScaleBytes, kScaleBytes, &M.bar[stage], policy);
     }
   };
   // Each warp's first pages into L2 while the previous kernel (normally
