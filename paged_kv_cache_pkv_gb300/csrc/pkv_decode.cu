@@ -632,6 +632,8 @@ __global__ void __launch_bounds__(F8 ? kDecWarpsF8 * 32 : kDecThreads, PKV_DEC_M
     const int g = pc.item / p.nsub;
     const size_t ph = size_t(pc.bid) * p.Hkv + g;  // (page, kv head)
     if (lane == 0) M.desc[stage] = StageDesc{pc.q0 + pc.j, pc.item, pc.item_start, pc.nvis - p.np * kPage};
+    // lane 0's store ordered before the arrival, whichever lane elect.sync picks
+    __syncwarp();
     mbar_arrive_expect_tx_w(&M.bar[stage], 2 * PB + (F8 ? 2 * kScaleBytes : 0));
     if (kDropFirstCopy && pc.item_start + pc.page == u_begin) return;
     // one box per page: the pool viewed as [units][128 bytes]; the host
