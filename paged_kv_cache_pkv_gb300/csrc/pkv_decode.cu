@@ -18,9 +18,9 @@
 //    and each decode warp takes an equal contiguous range, so 16-token and
 //    32768-token sequences are balanced to within one page.
 //  * Each warp is an independent worker with its own ring (2 stages for bf16
-//    pages, 3 for FP8): lane 0 issues the copies (L2 evict-first) that
-//    complete on an mbarrier; all 32 lanes compute.  No CTA barrier sits on
-//    the page loop.
+//    pages, 3 for FP8): the whole warp runs the copy issue and the lane
+//    elect.sync picks issues the copies (L2 evict-first) that complete on an
+//    mbarrier; all 32 lanes compute.  No CTA barrier sits on the page loop.
 //  * Page products on warp-level MMAs (mma.sync m16n8k16, f32 accumulators)
 //    fed straight from registers: S^T[16 tokens x 8 columns] = K . Q^T, then
 //    O^T[128 dims x 8 columns] += V^T . P^T.  Column c < GH is query head c
